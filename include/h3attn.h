@@ -1,0 +1,157 @@
+/*
+ * libh3attn -- the MiniMax-H3 / Wan video-DiT attention step on one GB300
+ * (sm_103a): fused Q/K RMSNorm + bf16 boundary + partial RoPE, then dense
+ * prefill attention.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are bf16, contiguous, in BSHD layout [batch, sequence, heads,
+ *   head_dim] (FastVideo PR #1832 "Add FlashInfer attention backend support
+ *   for MiniMax H3", section "Summary": query/key/value are
+ *   [batch, sequence, heads, head_dim]).  bf16 is passed as raw 16-bit words.
+ * - Pointers are DEVICE pointers unless stated otherwise.  The caller owns
+ *   every buffer; the library allocates no per-call memory.  It keeps one
+ *   4-byte device status word per device, created on the first call on that
+ *   device.
+ * - Every call is asynchronous on `stream` (0 = the legacy default stream).
+ *   Argument errors are detected on the host and returned before anything is
+ *   launched; nothing is written in that case.
+ * - Device-side bounded waits: the attention kernel never spins forever.  If
+ *   a pipeline wait exceeds its limit the kernel records H3ATTN_ERR_TIMEOUT
+ *   in the status word and returns; h3attn_check_device_status() reports it.
+ * - Inference only: there is no backward pass (FastVideo PR #1799 "Add
+ *   opt-in FlashInfer attention backend for Wan", section "Implementation":
+ *   grad-enabled inputs are rejected; the Python binding enforces that).
+ */
+#ifndef H3ATTN_H_
+#define H3ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque stream handle; pass a cudaStream_t. */
+typedef void* h3attn_stream_t;
+
+typedef enum {
+  H3ATTN_OK = 0,
+  H3ATTN_ERR_INVALID_ARG = 1,          /* null pointer, bad size, aliasing, causal with Sq != Sk, ... */
+  H3ATTN_ERR_MISALIGNED = 2,           /* a tensor pointer is not 16-byte aligned */
+  H3ATTN_ERR_UNSUPPORTED_HEAD_DIM = 3, /* head_dim not in {64, 128, 256} */
+  H3ATTN_ERR_UNSUPPORTED_DEVICE = 4,   /* current device is not compute capability 10.3 */
+  H3ATTN_ERR_UNSUPPORTED_MASK = 5,     /* mask form that has no representation here */
+  H3ATTN_ERR_LAUNCH = 6,               /* a CUDA runtime/driver call failed */
+  H3ATTN_ERR_TIMEOUT = 7               /* a device-side wait hit its limit (see check_device_status) */
+} h3attn_status_t;
+
+/*
+ * Attention mask descriptor.  Every field is an optional DEVICE pointer
+ * (NULL = absent), indexed per batch item and never per head: the pages'
+ * boolean [Q, K] custom mask is per batch item, and per-head [B, H, Q, K]
+ * masks are rejected (FastVideo PR #1799, sections "Implementation" and
+ * "Limitations").  The fields combine by logical AND of "may attend":
+ *
+ *   allowed(b, i, j) = j < Sk
+ *                    and (kv_len == NULL or j < kv_len[b])          key padding
+ *                    and (not causal_eff(b) or j <= i)               causal, top-left aligned
+ *                    and (bits == NULL or bit (j & 31) of bits[b, i, j >> 5])
+ *   causal_eff(b)    = causal argument != 0 or (causal_b != NULL and causal_b[b] != 0)
+ *
+ * kv_len[b] may be any int32: values <= 0 mask every key, values >= Sk mask
+ * none.  A query row with no allowed key produces an all-zero output row.
+ * q_len[b]: rows i >= q_len[b] of sample b are written as zeros (the
+ * fixed-valid zero-tail mode of TeleFuser PR #37 "perf(minimax-h3): optimize
+ * Ulysses attention and DiT kernels", sections 2.3 and 2.4).
+ * bits: uint32 words, shape [B, Sq, ceil(Sk / 32)], row-major, 4-byte
+ * aligned; bit value 1 = attend, and bits for j >= Sk are ignored.
+ */
+typedef struct {
+  const int32_t* kv_len;   /* [B] valid keys per sample, or NULL */
+  const int32_t* q_len;    /* [B] valid query rows per sample, or NULL */
+  const uint8_t* causal_b; /* [B] per-sample causal flag, or NULL */
+  const uint32_t* bits;    /* [B, Sq, ceil(Sk/32)] packed boolean mask, or NULL */
+} h3attn_mask_t;
+
+/*
+ * Fused Q/K RMSNorm -> bf16 rounding boundary -> partial rotate-half RoPE,
+ * IN PLACE on q and k.
+ *
+ * The step H3 runs on Q and K before attention: per-(token, head) RMSNorm,
+ * a BF16-compatible rounding, then RoPE on the first rotary_dim channels
+ * (FastVideo PR #1832, section "Preserve H3-specific attention behavior":
+ * H3 rotates 96 of its 128 head channels after Q/K RMSNorm; TeleFuser PR #37
+ * section 2.2, steps 1-3 of the fused kernel).  For every row x of D
+ * channels at sequence position s:
+ *   r      = 1 / sqrt(mean_d(x_d^2) + eps)
+ *   n_d    = bf16((x_d * r) * w_d)
+ *   for i < rotary_dim/2, with c = cos[s, i], t = sin[s, i], h = rotary_dim/2:
+ *     y_i     = n_i * c - n_{i+h} * t
+ *     y_{i+h} = n_{i+h} * c + n_i * t
+ *   y_d = n_d for d >= rotary_dim;  x <- bf16(y)
+ * The float32 operation order is fixed (lane partial sums of 8 channels,
+ * butterfly across lanes, correctly rounded sqrt and divide, separate
+ * multiplies, fused multiply-adds in the rotation, round-to-nearest-even
+ * stores), so results are reproducible bit for bit.
+ *
+ * q: [B, S, Hq, D] bf16, k: [B, S, Hkv, D] bf16 (device, in place, must not
+ *    overlap each other).  Either may be NULL with its head count 0 to
+ *    process only the other.
+ * wq, wk: [D] float32 RMSNorm weights (device), shared by all heads.
+ * cos, sin: [S, rotary_dim/2] float32 (device); row = sequence position.
+ *    May be NULL when rotary_dim == 0.
+ * D in {64, 128, 256}; rotary_dim a multiple of 16 with 0 <= rotary_dim <= D;
+ * eps >= 0 and finite.  Pointers 16-byte aligned (tables and weights 4-byte).
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_HEAD_DIM, UNSUPPORTED_DEVICE,
+ * LAUNCH.
+ */
+h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const float* wk,
+                                    const float* cos, const float* sin, int B, int S, int Hq,
+                                    int Hkv, int D, int rotary_dim, float eps,
+                                    h3attn_stream_t stream);
+
+/*
+ * Dense prefill attention  o = softmax(q k^T * scale) v  per (batch, query
+ * head), on BSHD bf16 tensors (FastVideo PR #1832, section "Summary": dense
+ * non-causal self-attention with head_dim 128; FastVideo PR #1799, section
+ * "Implementation": self- and cross-attention, MHA and GQA, causal,
+ * padding masks as a boolean [Q, K] mask, combined with causal when both are
+ * present; head dims 64, 128, 256).
+ *
+ * q: [B, Sq, Hq, D] bf16; k, v: [B, Sk, Hkv, D] bf16; o: [B, Sq, Hq, D] bf16
+ *    (all device; o must not overlap q, k or v).  Query head h reads key/value
+ *    head h / (Hq / Hkv) (GQA, contiguous groups).
+ * scale: finite, >= 0 (typically 1/sqrt(D)).
+ * mask: NULL (dense) or a descriptor as above.  causal: nonzero applies the
+ *    causal mask to every sample; causal masking requires Sq == Sk.
+ * D in {64, 128, 256}; Hq % Hkv == 0; B, Sq, Sk, Hq, Hkv >= 1 (B*Sq == 0 is
+ * a no-op).  Accumulation is float32 on the tensor cores; softmax in float32
+ * with exp2; the output is rounded once to bf16.
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_HEAD_DIM, UNSUPPORTED_DEVICE,
+ * UNSUPPORTED_MASK, LAUNCH.  A device-side pipeline timeout is reported by
+ * h3attn_check_device_status().
+ */
+h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Sq,
+                               int Sk, int Hq, int Hkv, int D, float scale,
+                               const h3attn_mask_t* mask, int causal, h3attn_stream_t stream);
+
+/* Static English description of a status code (never NULL). */
+const char* h3attn_status_string(h3attn_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns H3ATTN_ERR_TIMEOUT if any kernel since the last check gave
+ * up on a bounded wait, H3ATTN_ERR_LAUNCH if the stream reports a CUDA error,
+ * else H3ATTN_OK.
+ */
+h3attn_status_t h3attn_check_device_status(h3attn_stream_t stream);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int h3attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3ATTN_H_ */

@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; host-side argument validation answers before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import video_dit_dense_gb300 as h3
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "h3attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    h3.build()
+    return h3.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(h3attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("h3attn_qk_norm_rope", "h3attn_prefill", "h3attn_status_string",
+              "h3attn_check_device_status", "h3attn_version"):
+        assert n in names
+    assert set(names) == set(h3.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", h3.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(h3attn_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.h3attn_version() == 10000
+    for code in range(8):
+        s = lib.h3attn_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.h3attn_status_string(99).decode() == "unknown status"
+
+
+FAKE = 0x10000  # 16-byte aligned fake device address; validation fails before any use
+
+
+def prefill(lib, q=FAKE, k=FAKE * 2, v=FAKE * 3, o=FAKE * 4, B=1, Sq=256, Sk=256, Hq=4, Hkv=4, D=128,
+            scale=0.088, mask=None, causal=0):
+    return lib.h3attn_prefill(q, k, v, o, B, Sq, Sk, Hq, Hkv, D, scale, mask, causal, None)
+
+
+def test_prefill_validation(lib):
+    assert prefill(lib, D=96) == h3.H3ATTN_ERR_UNSUPPORTED_HEAD_DIM
+    assert prefill(lib, D=512) == h3.H3ATTN_ERR_UNSUPPORTED_HEAD_DIM
+    assert prefill(lib, Hq=6, Hkv=4) == h3.H3ATTN_ERR_INVALID_ARG
+    assert prefill(lib, scale=-1.0) == h3.H3ATTN_ERR_INVALID_ARG
+    assert prefill(lib, scale=float("nan")) == h3.H3ATTN_ERR_INVALID_ARG
+    assert prefill(lib, scale=0.0) == h3.H3ATTN_ERR_INVALID_ARG
+    assert prefill(lib, Sk=0) == h3.H3ATTN_ERR_INVALID_ARG
+    assert prefill(lib, Sq=100, Sk=200, causal=1) == h3.H3ATTN_ERR_INVALID_ARG
+    m = h3.h3attn_mask_t(None, None, FAKE, None)
+    assert prefill(lib, Sq=100, Sk=200, mask=ctypes.pointer(m)) == h3.H3ATTN_ERR_INVALID_ARG
+    assert prefill(lib, q=FAKE + 8) == h3.H3ATTN_ERR_MISALIGNED
+    assert prefill(lib, o=FAKE * 4 + 2) == h3.H3ATTN_ERR_MISALIGNED
+    m = h3.h3attn_mask_t(None, None, None, FAKE + 2)
+    assert prefill(lib, mask=ctypes.pointer(m)) == h3.H3ATTN_ERR_MISALIGNED
+    assert prefill(lib, q=None) == h3.H3ATTN_ERR_INVALID_ARG
+    assert prefill(lib, o=FAKE) == h3.H3ATTN_ERR_INVALID_ARG  # o aliases q
+    assert prefill(lib, B=0) == h3.H3ATTN_OK  # empty batch: no-op, nothing launched
+    assert prefill(lib, Sq=0) == h3.H3ATTN_OK
+
+
+def norm(lib, q=FAKE, k=FAKE * 64, wq=FAKE * 200, wk=FAKE * 201, cos=FAKE * 202, sin=FAKE * 203, B=1, S=16,
+         Hq=2, Hkv=2, D=128, rot=96, eps=1e-6):
+    return lib.h3attn_qk_norm_rope(q, k, wq, wk, cos, sin, B, S, Hq, Hkv, D, rot, eps, None)
+
+
+def test_norm_rope_validation(lib):
+    assert norm(lib, D=80) == h3.H3ATTN_ERR_UNSUPPORTED_HEAD_DIM
+    assert norm(lib, rot=100) == h3.H3ATTN_ERR_INVALID_ARG  # not a multiple of 16
+    assert norm(lib, rot=144) == h3.H3ATTN_ERR_INVALID_ARG  # > D
+    assert norm(lib, eps=-1.0) == h3.H3ATTN_ERR_INVALID_ARG
+    assert norm(lib, eps=float("inf")) == h3.H3ATTN_ERR_INVALID_ARG
+    assert norm(lib, cos=None) == h3.H3ATTN_ERR_INVALID_ARG
+    assert norm(lib, wq=None) == h3.H3ATTN_ERR_INVALID_ARG
+    assert norm(lib, q=None) == h3.H3ATTN_ERR_INVALID_ARG  # q absent but Hq > 0
+    assert norm(lib, q=FAKE + 4) == h3.H3ATTN_ERR_MISALIGNED
+    assert norm(lib, cos=FAKE * 202 + 4) == h3.H3ATTN_ERR_MISALIGNED
+    assert norm(lib, k=FAKE + 256) == h3.H3ATTN_ERR_INVALID_ARG  # k overlaps q
+    assert norm(lib, B=0) == h3.H3ATTN_OK
+    assert norm(lib, q=None, Hq=0, k=None, Hkv=0) == h3.H3ATTN_OK

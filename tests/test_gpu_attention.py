@@ -1,0 +1,151 @@
+"""GPU parity of the prefill attention kernel against the fp64 oracle, called
+through the C ABI.  Full comparison where the oracle finishes in seconds;
+sampled rows (each row is independent, so a sampled row is compared
+exactly) at the full workload sizes, in the same launch configuration the
+bench times.  Bound: max |err| <= 2e-2 and relative RMS <= 5e-3."""
+import numpy as np
+import pytest
+
+import h3inputs as gen
+import oracle
+from helpers import (check_close, from_dev, sample_rows, to_dev, to_dev_f32, to_dev_i32, to_dev_u8)
+
+
+def gpu_attention(h3, q, k, v, scale, causal=False, kv_len=None, q_len=None, causal_b=None, bits=None):
+    import torch
+    dq, dk, dv = to_dev(q), to_dev(k), to_dev(v)
+    do = torch.full(dq.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    mask = None
+    if any(x is not None for x in (kv_len, q_len, causal_b, bits)):
+        mask = h3.Mask(kv_len=None if kv_len is None else to_dev_i32(kv_len),
+                       q_len=None if q_len is None else to_dev_i32(q_len),
+                       causal_b=None if causal_b is None else to_dev_u8(causal_b),
+                       bits=None if bits is None else torch.from_numpy(bits.view(np.int32)).cuda())
+    h3.h3attn_prefill(dq, dk, dv, do, scale, mask, causal)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    return from_dev(do)
+
+
+def full_case(h3, B, Sq, Sk, Hq, Hkv, D, seed=0, causal=False, kv_len=None, q_len=None, causal_b=None,
+              bits_density=None, std=1.0, what=""):
+    q = gen.normal_bshd(B, Sq, Hq, D, seed, gen.STREAM_Q, std)
+    k = gen.normal_bshd(B, Sk, Hkv, D, seed, gen.STREAM_K, std)
+    v = gen.normal_bshd(B, Sk, Hkv, D, seed, gen.STREAM_V)
+    bits = None if bits_density is None else gen.bernoulli_bits(B, Sq, Sk, seed, gen.STREAM_BITS, bits_density)
+    scale = 1.0 / np.sqrt(D)
+    got = gpu_attention(h3, q, k, v, scale, causal, kv_len, q_len, causal_b, bits)
+    ref = oracle.attention_f64(q, k, v, scale, causal, kv_len, q_len, causal_b, bits)
+    return check_close(got, ref, what)
+
+
+# ---------------------------------------------------------------- small / edge cases
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,Sq,Sk,Hq,Hkv,D", [
+    (1, 128, 128, 1, 1, 128),    # one tile
+    (1, 256, 256, 2, 2, 128),    # one CTA, two query tiles
+    (1, 300, 300, 2, 2, 128),    # ragged query and key tails
+    (2, 77, 200, 4, 2, 128),     # cross-attention + GQA, short query
+    (1, 1, 1, 1, 1, 128),        # single row, single key
+    (1, 513, 129, 3, 1, 128),    # ragged both sides, MQA
+    (1, 190, 333, 2, 2, 64),
+    (2, 130, 260, 4, 2, 256),
+])
+def test_dense_shapes(h3, B, Sq, Sk, Hq, Hkv, D):
+    full_case(h3, B, Sq, Sk, Hq, Hkv, D, seed=B * 1000 + Sq, what=f"dense {B},{Sq},{Sk},{Hq},{Hkv},{D}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_causal_and_padding(h3, D):
+    B, S = 3, 389
+    kv_len = np.array([389, 150, 1], np.int32)
+    causal_b = np.array([1, 0, 1], np.uint8)
+    full_case(h3, B, S, S, 4, 2, D, seed=3, kv_len=kv_len, causal_b=causal_b, what=f"causal+pad D={D}")
+    full_case(h3, 1, 300, 300, 2, 1, D, seed=4, causal=True, what=f"causal D={D}")
+
+
+@pytest.mark.gpu
+def test_bit_mask_and_q_len_and_degenerate(h3):
+    # random packed boolean [Q, K] mask, combined with key padding
+    full_case(h3, 2, 200, 333, 2, 2, 128, seed=5, bits_density=0.3, kv_len=np.array([333, 100], np.int32),
+              what="bits+pad")
+    # very sparse mask: many rows fully masked -> zero rows
+    full_case(h3, 1, 140, 140, 2, 2, 128, seed=6, bits_density=0.002, what="sparse bits")
+    # zero-tail mode and kv_len <= 0 (every key masked -> zeros)
+    full_case(h3, 3, 270, 270, 2, 2, 128, seed=7, q_len=np.array([270, 13, 0], np.int32),
+              kv_len=np.array([-5, 270, 100], np.int32), what="q_len/kv_len edge")
+
+
+@pytest.mark.gpu
+def test_peaky_scores_exercise_rescaling(h3):
+    """Large-magnitude inputs: maxima grow across key tiles, forcing O rescales."""
+    full_case(h3, 1, 256, 1024, 2, 2, 128, seed=8, std=4.0, what="peaky")
+
+
+@pytest.mark.gpu
+def test_gqa_equals_repeated_heads_on_gpu(h3):
+    B, S, Hq, Hkv, D = 1, 256, 8, 2, 128
+    q = gen.normal_bshd(B, S, Hq, D, 9, gen.STREAM_Q)
+    k = gen.normal_bshd(B, S, Hkv, D, 9, gen.STREAM_K)
+    v = gen.normal_bshd(B, S, Hkv, D, 9, gen.STREAM_V)
+    o1 = gpu_attention(h3, q, k, v, 0.1)
+    o2 = gpu_attention(h3, q, np.repeat(k, 4, axis=2).copy(), np.repeat(v, 4, axis=2).copy(), 0.1)
+    np.testing.assert_array_equal(o1, o2)
+
+
+# ---------------------------------------------------------------- the workloads
+def _workload_inputs(name, seed):
+    wl = gen.WORKLOADS[name]
+    inp = gen.make_inputs(wl, seed)
+    q, k = inp.q, inp.k
+    if wl.norm_rope:
+        # The attention oracle consumes the oracle's own norm/RoPE output
+        # (the GPU kernel is bit-exact to it, see test_gpu_norm_rope.py).
+        q = oracle.qk_norm_rope_emulate(inp.q, inp.wq, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+        if not wl.cross:
+            k = oracle.qk_norm_rope_emulate(inp.k, inp.wk, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+    return wl, inp, q, k
+
+
+def _gpu_step(h3, wl, inp):
+    """The whole step on the GPU: norm/RoPE in place, then attention."""
+    import torch
+    dq, dk, dv = to_dev(inp.q), to_dev(inp.k), to_dev(inp.v)
+    if wl.norm_rope:
+        h3.h3attn_qk_norm_rope(dq, None if wl.cross else dk, to_dev_f32(inp.wq),
+                               None if wl.cross else to_dev_f32(inp.wk), to_dev_f32(inp.cos),
+                               to_dev_f32(inp.sin), wl.rotary_dim, wl.eps)
+    mask = None
+    if inp.kv_len is not None or inp.causal_b is not None:
+        mask = h3.Mask(kv_len=None if inp.kv_len is None else to_dev_i32(inp.kv_len),
+                       causal_b=None if inp.causal_b is None else to_dev_u8(inp.causal_b))
+    do = torch.empty_like(dq)
+    h3.h3attn_prefill(dq, dk, dv, do, wl.scale, mask, False)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    return from_dev(do)
+
+
+FULL = ["tiny_mha", "dit_block", "padded_gqa_d64", "padded_gqa_d256"]
+SAMPLED = {"long_video_h12": 24, "long_video_h24": 8, "padded_gqa": 24, "packed_clip_self": 8,
+           "packed_clip_cross": 48}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", FULL)
+def test_workload_full(h3, name):
+    wl, inp, q, k = _workload_inputs(name, seed=0)
+    got = _gpu_step(h3, wl, inp)
+    ref = oracle.attention_f64(q, k, inp.v, wl.scale, False, inp.kv_len, None, inp.causal_b)
+    check_close(got, ref, name)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", list(SAMPLED))
+def test_workload_sampled_rows(h3, name):
+    wl, inp, q, k = _workload_inputs(name, seed=1234)
+    got = _gpu_step(h3, wl, inp)
+    ids = sample_rows(wl.B, wl.Sq, wl.Hq, SAMPLED[name], seed=1, kv_len=inp.kv_len)
+    ref = oracle.attention_f64(q, k, inp.v, wl.scale, False, inp.kv_len, None, inp.causal_b, row_ids=ids)
+    check_close(got.reshape(-1, wl.D)[ids], ref, name)

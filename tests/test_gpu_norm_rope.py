@@ -1,0 +1,87 @@
+"""GPU parity of the fused Q/K RMSNorm + bf16 boundary + partial RoPE kernel:
+bit-exact against the oracle's float32 fixed-order emulation, called through
+the C ABI, on every workload that runs the step and on edge cases."""
+import numpy as np
+import pytest
+
+import h3inputs as gen
+import oracle
+from helpers import from_dev, to_dev, to_dev_f32
+
+NORM_WORKLOADS = ["tiny_mha", "dit_block", "long_video_h12", "padded_gqa", "packed_clip_self"]
+
+
+def _run(h3, q_bits, k_bits, wq, wk, cos, sin, rot, eps):
+    import torch
+    q = to_dev(q_bits) if q_bits is not None else None
+    k = to_dev(k_bits) if k_bits is not None else None
+    h3.h3attn_qk_norm_rope(q, k, to_dev_f32(wq) if wq is not None else None,
+                           to_dev_f32(wk) if wk is not None else None,
+                           to_dev_f32(cos) if cos is not None else None,
+                           to_dev_f32(sin) if sin is not None else None, rot, eps)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    return (from_dev(q) if q is not None else None), (from_dev(k) if k is not None else None)
+
+
+def _assert_bits_equal(got, ref, what):
+    bad = np.flatnonzero(got.reshape(-1) != ref.reshape(-1))
+    assert bad.size == 0, f"{what}: {bad.size} of {got.size} elements differ, first at flat index {bad[:5]}"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", NORM_WORKLOADS)
+def test_bit_exact_on_workloads(h3, name):
+    wl = gen.WORKLOADS[name]
+    inp = gen.make_inputs(wl, seed=42)
+    gq, gk = _run(h3, inp.q, inp.k, inp.wq, inp.wk, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+    _assert_bits_equal(gq, oracle.qk_norm_rope_emulate(inp.q, inp.wq, inp.cos, inp.sin, wl.rotary_dim, wl.eps),
+                       f"{name} q")
+    _assert_bits_equal(gk, oracle.qk_norm_rope_emulate(inp.k, inp.wk, inp.cos, inp.sin, wl.rotary_dim, wl.eps),
+                       f"{name} k")
+
+
+@pytest.mark.gpu
+def test_bit_exact_cross_attention_query_only(h3):
+    wl = gen.WORKLOADS["packed_clip_cross"]
+    inp = gen.make_inputs(wl, seed=0)
+    gq, _ = _run(h3, inp.q, None, inp.wq, None, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+    _assert_bits_equal(gq, oracle.qk_norm_rope_emulate(inp.q, inp.wq, inp.cos, inp.sin, wl.rotary_dim, wl.eps),
+                       "cross q")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,rot,eps,B,S,Hq,Hkv", [
+    (128, 96, 1e-6, 2, 37, 3, 1),     # ragged rows, GQA head counts
+    (128, 128, 1e-6, 1, 64, 4, 4),    # full rotation
+    (128, 0, 1e-6, 1, 64, 4, 4),      # norm only
+    (128, 32, 1e-2, 1, 50, 2, 2),     # short rotation, large eps
+    (64, 32, 1e-6, 3, 33, 4, 2),
+    (64, 64, 0.0, 1, 31, 2, 2),
+    (256, 96, 1e-6, 2, 29, 2, 2),
+    (256, 256, 1e-6, 1, 17, 3, 3),
+])
+def test_bit_exact_edge_shapes(h3, D, rot, eps, B, S, Hq, Hkv):
+    q = gen.normal_bshd(B, S, Hq, D, 7, gen.STREAM_Q, 2.0, 0.5)
+    k = gen.normal_bshd(B, S, Hkv, D, 7, gen.STREAM_K, 0.25, 0.0)
+    wq = gen.uniform_f32(D, 7, gen.STREAM_WQ, 0.5, 1.5)
+    wk = gen.uniform_f32(D, 7, gen.STREAM_WK, 0.5, 1.5)
+    cos, sin = gen.rope_tables(S, rot) if rot else (None, None)
+    gq, gk = _run(h3, q, k, wq, wk, cos, sin, rot, eps)
+    _assert_bits_equal(gq, oracle.qk_norm_rope_emulate(q, wq, cos, sin, rot, eps), "q")
+    _assert_bits_equal(gk, oracle.qk_norm_rope_emulate(k, wk, cos, sin, rot, eps), "k")
+
+
+@pytest.mark.gpu
+def test_zero_rows_and_tiny_values(h3):
+    """Rows of zeros (r = 1/sqrt(eps)) and subnormal-scale inputs."""
+    D, S = 128, 8
+    q = gen.normal_bshd(1, S, 2, D, 3, gen.STREAM_Q)
+    q[0, 0] = 0
+    q[0, 1, 0] = 0x0001  # tiniest subnormal bf16
+    k = (gen.normal_bshd(1, S, 2, D, 3, gen.STREAM_K).astype(np.uint32) & 0x80FF) .astype(np.uint16)  # tiny values
+    w = gen.uniform_f32(D, 3, gen.STREAM_WQ, 0.5, 1.5)
+    cos, sin = gen.rope_tables(S, 96)
+    gq, gk = _run(h3, q, k, w, w, cos, sin, 96, 1e-6)
+    _assert_bits_equal(gq, oracle.qk_norm_rope_emulate(q, w, cos, sin, 96, 1e-6), "q")
+    _assert_bits_equal(gk, oracle.qk_norm_rope_emulate(k, w, cos, sin, 96, 1e-6), "k")

@@ -1,0 +1,206 @@
+"""Thin ctypes binding of libh3attn (the H3 attention step on one GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libh3attn.so``.  PyTorch supplies device memory and streams.
+There is no CPU or eager fallback: if the library is missing or the device
+is not sm_103, calls raise.
+
+The two entry points mirror the C ABI in ``include/h3attn.h``:
+
+* ``h3attn_qk_norm_rope(q, k, wq, wk, cos, sin, rotary_dim, eps, stream)`` --
+  fused Q/K RMSNorm, bf16 boundary and partial RoPE, in place (FastVideo
+  PR #1832 "Add FlashInfer attention backend support for MiniMax H3",
+  section "Preserve H3-specific attention behavior").
+* ``h3attn_prefill(q, k, v, o, scale, mask, causal, stream)`` -- dense
+  prefill attention on BSHD bf16 tensors with GQA, cross-attention, causal
+  and boolean-mask variants (FastVideo PR #1799 "Add opt-in FlashInfer
+  attention backend for Wan", section "Implementation").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libh3attn.so")
+
+H3ATTN_OK = 0
+H3ATTN_ERR_INVALID_ARG = 1
+H3ATTN_ERR_MISALIGNED = 2
+H3ATTN_ERR_UNSUPPORTED_HEAD_DIM = 3
+H3ATTN_ERR_UNSUPPORTED_DEVICE = 4
+H3ATTN_ERR_UNSUPPORTED_MASK = 5
+H3ATTN_ERR_LAUNCH = 6
+H3ATTN_ERR_TIMEOUT = 7
+
+# Every symbol include/h3attn.h declares.
+EXPORTED = ("h3attn_qk_norm_rope", "h3attn_prefill", "h3attn_status_string",
+            "h3attn_check_device_status", "h3attn_version")
+
+
+class H3AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.h3attn_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+class h3attn_mask_t(ctypes.Structure):
+    _fields_ = [("kv_len", ctypes.c_void_p), ("q_len", ctypes.c_void_p),
+                ("causal_b", ctypes.c_void_p), ("bits", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libh3attn.so for sm_103a in this directory."""
+    from . import _build
+    return _build.build(force=force, verbose=verbose)
+
+
+def load(path: str = LIB_PATH):
+    """Load libh3attn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with video_dit_dense_gb300.build()")
+            lib = ctypes.CDLL(path)
+            P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            lib.h3attn_qk_norm_rope.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+            lib.h3attn_qk_norm_rope.restype = I
+            lib.h3attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, F,
+                                           ctypes.POINTER(h3attn_mask_t), I, P]
+            lib.h3attn_prefill.restype = I
+            lib.h3attn_status_string.argtypes = [I]
+            lib.h3attn_status_string.restype = ctypes.c_char_p
+            lib.h3attn_check_device_status.argtypes = [P]
+            lib.h3attn_check_device_status.restype = I
+            lib.h3attn_version.argtypes = []
+            lib.h3attn_version.restype = I
+            _lib = lib
+    return _lib
+
+
+def lib():
+    return load()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_bf16(name, t):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must be a contiguous 4-D bf16 CUDA tensor (BSHD)")
+    if t.requires_grad:
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name}: inference only, grad-enabled inputs are rejected")
+
+
+def _raise_if(status, where):
+    if status != H3ATTN_OK:
+        raise H3AttnError(status, where)
+
+
+def h3attn_qk_norm_rope(q, k, wq, wk, cos, sin, rotary_dim=96, eps=1e-6, stream=None):
+    """In-place fused Q/K RMSNorm + bf16 boundary + partial RoPE.
+
+    q: [B, S, Hq, D] bf16, k: [B, S, Hkv, D] bf16 (either may be None);
+    wq, wk: [D] float32; cos, sin: [>=S, rotary_dim/2] float32.
+    """
+    load()
+    ref = q if q is not None else k
+    if q is not None:
+        _check_bf16("q", q)
+    if k is not None:
+        _check_bf16("k", k)
+    B, S, _, D = ref.shape
+    Hq = q.shape[2] if q is not None else 0
+    Hkv = k.shape[2] if k is not None else 0
+    if k is not None and q is not None and (k.shape[0], k.shape[1], k.shape[3]) != (B, S, D):
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "q and k must share batch, sequence and head_dim")
+    import torch
+    for name, t in (("wq", wq), ("wk", wk), ("cos", cos), ("sin", sin)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()):
+            raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must be a contiguous float32 CUDA tensor")
+    if rotary_dim > 0 and (cos.shape[-1] != rotary_dim // 2 or cos.numel() < S * (rotary_dim // 2)
+                           or sin.shape != cos.shape):
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "cos/sin must be [>=S, rotary_dim/2]")
+    st = _lib.h3attn_qk_norm_rope(_ptr(q), _ptr(k), _ptr(wq), _ptr(wk), _ptr(cos), _ptr(sin),
+                                  B, S, Hq, Hkv, D, int(rotary_dim), float(eps), _stream_handle(stream))
+    _raise_if(st, "h3attn_qk_norm_rope")
+
+
+@dataclass
+class Mask:
+    """Mask descriptor (device tensors, per batch item): see h3attn_mask_t."""
+    kv_len: object = None    # int32 [B]
+    q_len: object = None     # int32 [B]
+    causal_b: object = None  # uint8 [B]
+    bits: object = None      # int32/uint32 [B, Sq, ceil(Sk/32)]
+
+
+def h3attn_prefill(q, k, v, o, scale=None, mask: Mask | None = None, causal=False, stream=None):
+    """o <- softmax(q k^T * scale) v on BSHD bf16 tensors (o preallocated)."""
+    load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_bf16(name, t)
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or tuple(o.shape) != tuple(q.shape):
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "shape mismatch between q, k, v and o")
+    if scale is None:
+        scale = 1.0 / float(D) ** 0.5
+    mptr = None
+    if mask is not None:
+        import torch
+        if mask.bits is not None:
+            if mask.bits.dim() == 4:
+                raise H3AttnError(H3ATTN_ERR_UNSUPPORTED_MASK, "per-head [B, H, Q, K] masks are not supported")
+            W = (Sk + 31) // 32
+            if tuple(mask.bits.shape) != (B, Sq, W) or mask.bits.element_size() != 4:
+                raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"bits must be 32-bit words of shape [{B}, {Sq}, {W}]")
+        for name, t, dt in (("kv_len", mask.kv_len, torch.int32), ("q_len", mask.q_len, torch.int32),
+                            ("causal_b", mask.causal_b, torch.uint8)):
+            if t is not None and (t.dtype != dt or t.numel() != B or not t.is_cuda):
+                raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must be a [{B}] {dt} CUDA tensor")
+        m = h3attn_mask_t(_ptr(mask.kv_len), _ptr(mask.q_len), _ptr(mask.causal_b), _ptr(mask.bits))
+        mptr = ctypes.pointer(m)
+    st = _lib.h3attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Sq, Sk, Hq, Hkv, D, float(scale), mptr,
+                             int(bool(causal)), _stream_handle(stream))
+    _raise_if(st, "h3attn_prefill")
+    return o
+
+
+def h3attn_check_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    load()
+    return _lib.h3attn_check_device_status(_stream_handle(stream))
+
+
+def h3attn_status_string(status: int) -> str:
+    return load().h3attn_status_string(status).decode()
+
+
+def h3attn_version() -> int:
+    return load().h3attn_version()
+
+
+# Short aliases.
+qk_norm_rope = h3attn_qk_norm_rope
+prefill = h3attn_prefill
+check_device_status = h3attn_check_device_status

@@ -1,0 +1,200 @@
+// C-ABI entry points of libh3attn: argument validation, device gate, TMA
+// descriptor construction and error mapping.  No entry point allocates
+// device memory; all work is enqueued on the caller's stream.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::once_flag once;
+  bool supported = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Gate on compute capability 10.3 (the only target the kernels are built for).
+h3attn_status_t check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return H3ATTN_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return H3ATTN_ERR_UNSUPPORTED_DEVICE;
+  std::call_once(g_dev[dev].once, [dev]() {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return;
+    g_dev[dev].supported = (major == 10 && minor == 3);
+  });
+  return g_dev[dev].supported ? H3ATTN_OK : H3ATTN_ERR_UNSUPPORTED_DEVICE;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(nb) && b0 < a0 + static_cast<uintptr_t>(na);
+}
+
+// 4-D map over a BSHD bf16 tensor: dims (D, H, S, B), box (64, 1, 128, 1),
+// 128-byte swizzle, zero fill outside the tensor.
+bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(S) * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(h3::kBlockM), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+uint64_t wait_limit_ns() {
+  const char* s = getenv("H3ATTN_WAIT_LIMIT_MS");
+  long ms = s ? strtol(s, nullptr, 10) : 0;
+  if (ms <= 0) ms = 2000;
+  return static_cast<uint64_t>(ms) * 1000000ull;
+}
+
+bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
+
+}  // namespace
+
+extern "C" {
+
+int h3attn_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* h3attn_status_string(h3attn_status_t s) {
+  switch (s) {
+    case H3ATTN_OK: return "ok";
+    case H3ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case H3ATTN_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case H3ATTN_ERR_UNSUPPORTED_HEAD_DIM: return "unsupported head dimension (64, 128 or 256)";
+    case H3ATTN_ERR_UNSUPPORTED_DEVICE: return "unsupported device (compute capability 10.3 required)";
+    case H3ATTN_ERR_UNSUPPORTED_MASK: return "unsupported mask form";
+    case H3ATTN_ERR_LAUNCH: return "CUDA launch or runtime error";
+    case H3ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const float* wk,
+                                    const float* cos, const float* sin, int B, int S, int Hq,
+                                    int Hkv, int D, int rotary_dim, float eps,
+                                    h3attn_stream_t stream) {
+  if (B < 0 || S < 0 || Hq < 0 || Hkv < 0) return H3ATTN_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return H3ATTN_ERR_UNSUPPORTED_HEAD_DIM;
+  if (rotary_dim < 0 || rotary_dim > D || rotary_dim % 16 != 0) return H3ATTN_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !isfinite(eps)) return H3ATTN_ERR_INVALID_ARG;
+  if ((q == nullptr) != (Hq == 0) || (k == nullptr) != (Hkv == 0)) return H3ATTN_ERR_INVALID_ARG;
+  if (q && !wq) return H3ATTN_ERR_INVALID_ARG;
+  if (k && !wk) return H3ATTN_ERR_INVALID_ARG;
+  if (rotary_dim > 0 && (!cos || !sin)) return H3ATTN_ERR_INVALID_ARG;
+  const int64_t rows_q = static_cast<int64_t>(B) * S * Hq;
+  const int64_t rows_k = static_cast<int64_t>(B) * S * Hkv;
+  if (rows_q + rows_k == 0) return H3ATTN_OK;
+  if ((q && !aligned16(q)) || (k && !aligned16(k)) || (wq && !aligned16(wq)) ||
+      (wk && !aligned16(wk)) || (cos && !aligned16(cos)) || (sin && !aligned16(sin)))
+    return H3ATTN_ERR_MISALIGNED;
+  if (q && k && overlap(q, rows_q * D * 2, k, rows_k * D * 2)) return H3ATTN_ERR_INVALID_ARG;
+  h3attn_status_t st = check_device();
+  if (st != H3ATTN_OK) return st;
+  h3::NormRopeArgs a;
+  a.q = static_cast<uint16_t*>(q);
+  a.k = static_cast<uint16_t*>(k);
+  a.wq = wq;
+  a.wk = wk;
+  a.cos = cos;
+  a.sin = sin;
+  a.rows_q = rows_q;
+  a.rows_k = rows_k;
+  a.S = S;
+  a.Hq = Hq > 0 ? Hq : 1;
+  a.Hkv = Hkv > 0 ? Hkv : 1;
+  a.D = D;
+  a.rotary_dim = rotary_dim;
+  a.eps = eps;
+  cudaError_t e = h3::launch_qk_norm_rope(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_LAUNCH;
+}
+
+h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Sq,
+                               int Sk, int Hq, int Hkv, int D, float scale,
+                               const h3attn_mask_t* mask, int causal, h3attn_stream_t stream) {
+  if (B < 0 || Sq < 0 || Sk < 1 || Hq < 1 || Hkv < 1) return H3ATTN_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return H3ATTN_ERR_UNSUPPORTED_HEAD_DIM;
+  if (Hq % Hkv != 0) return H3ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || !isfinite(scale)) return H3ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535) return H3ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return H3ATTN_OK;
+  if (!q || !k || !v || !o) return H3ATTN_ERR_INVALID_ARG;
+  const bool any_causal = causal || (mask && mask->causal_b);
+  if (any_causal && Sq != Sk) return H3ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return H3ATTN_ERR_MISALIGNED;
+  if (mask && mask->bits && (reinterpret_cast<uintptr_t>(mask->bits) & 3u))
+    return H3ATTN_ERR_MISALIGNED;
+  if (mask && ((mask->kv_len && (reinterpret_cast<uintptr_t>(mask->kv_len) & 3u)) ||
+               (mask->q_len && (reinterpret_cast<uintptr_t>(mask->q_len) & 3u))))
+    return H3ATTN_ERR_MISALIGNED;
+  const int64_t nq = static_cast<int64_t>(B) * Sq * Hq * D * 2;
+  const int64_t nk = static_cast<int64_t>(B) * Sk * Hkv * D * 2;
+  if (overlap(o, nq, q, nq) || overlap(o, nq, k, nk) || overlap(o, nq, v, nk))
+    return H3ATTN_ERR_INVALID_ARG;
+  h3attn_status_t st = check_device();
+  if (st != H3ATTN_OK) return st;
+
+  h3::AttnArgs a;
+  if (!make_bshd_map(&a.tm_q, q, B, Sq, Hq, D) || !make_bshd_map(&a.tm_k, k, B, Sk, Hkv, D) ||
+      !make_bshd_map(&a.tm_v, v, B, Sk, Hkv, D))
+    return H3ATTN_ERR_LAUNCH;
+  a.o = static_cast<uint16_t*>(o);
+  a.kv_len = mask ? mask->kv_len : nullptr;
+  a.q_len = mask ? mask->q_len : nullptr;
+  a.causal_b = mask ? mask->causal_b : nullptr;
+  a.bits = mask ? mask->bits : nullptr;
+  a.B = B;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = wait_limit_ns();
+  const char* inj = getenv("H3ATTN_FAULT_INJECT_STALL_PRODUCER");
+  a.debug_skip_producer = (inj && inj[0] == '1') ? 1 : 0;
+  cudaError_t e = h3::launch_attention(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_LAUNCH;
+}
+
+h3attn_status_t h3attn_check_device_status(h3attn_stream_t stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return H3ATTN_ERR_LAUNCH;
+  int v = 0;
+  if (h3::read_and_clear_status(&v) != 0) return H3ATTN_ERR_LAUNCH;
+  return v == 0 ? H3ATTN_OK : static_cast<h3attn_status_t>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,432 @@
+// Dense prefill attention o = softmax(q k^T * scale) v on BSHD bf16 tensors
+// for sm_103a (FastVideo PR #1832 "Add FlashInfer attention backend support
+// for MiniMax H3", section "Summary": dense non-causal self-attention on
+// [batch, sequence, heads, head_dim] with head_dim 128; FastVideo PR #1799
+// "Add opt-in FlashInfer attention backend for Wan", section
+// "Implementation": cross-attention, GQA, causal and boolean [Q, K] masks).
+//
+// One CTA owns NQ query tiles of 128 rows of one (batch, head) and streams
+// that head's K/V through shared memory in 128-key tiles:
+//
+//   warp 4*NQ      TMA producer: Q tiles once, then K_j, V_j into a ring of
+//                  NSTAGE shared-memory stages (mbarrier full/empty pairs).
+//   warp 4*NQ+1    MMA issuer (one thread): S_q = Q_q K_j^T with
+//                  tcgen05.mma (both operands in shared memory, fp32
+//                  accumulator in tensor memory), then O_q += P_q V_j with
+//                  P_q read from tensor memory.  Also allocates tensor memory.
+//   warps 4q..4q+3 softmax warpgroup of tile q: thread t owns query row t
+//                  (tensor-memory lane t).  It reads its 128 scores, applies
+//                  the mask, keeps a running max and sum, writes
+//                  P = exp2(s*scale*log2e - m) as bf16 back into tensor
+//                  memory over the scores, rescales its O row when the max
+//                  grows by more than 2^8, and finally writes O / l.
+//
+// Tensor memory (512 columns x 128 lanes): S_q at columns [128q, 128q+128),
+// P_q over the first 64 columns of S_q (bf16 pairs), O_q at
+// [128*NQ + D*q, 128*NQ + D*(q+1)).
+//
+// The next S_q = Q_q K^T overwrites P_q, and tcgen05 only orders MMAs that
+// share an accumulator, so the issuer waits for O_q += P_q V to complete
+// before it issues the next S_q; the other tile's MMA is queued meanwhile,
+// which keeps the tensor pipe busy across that wait.
+//
+// Masking: tiles entirely inside the allowed region run unmasked; the
+// kv_len boundary tile, causal diagonal tiles and every tile of a packed-bit
+// mask set disallowed scores to -inf before the max.  Key tiles past the
+// last allowed key of the CTA are never loaded.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace h3 {
+namespace {
+
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+
+template <int D, int NQ, int NSTAGE>
+struct Cfg {
+  static constexpr int kChunks = D / 64;                  // 128-byte swizzle columns per row
+  static constexpr int kTileBytes = kBlockM * D * 2;      // one 128-row tile of Q, K or V
+  static constexpr int kChunkBytes = kBlockM * 128;       // 16 KiB: one swizzle column of a tile
+  static constexpr int kSmemQ = NQ * kTileBytes;
+  static constexpr int kSmemKV = NSTAGE * kTileBytes;
+  static constexpr int kNumBars = 1 + 2 * NSTAGE + 3 * NQ + 1;
+  static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kSmemQ + kSmemKV + kNumBars * 8 + 16;
+  static constexpr int kThreads = NQ * 128 + 64;
+  static constexpr int kProducerWarp = NQ * 4;
+  static constexpr int kMmaWarp = NQ * 4 + 1;
+  static constexpr int kColO = NQ * 128;
+  static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kBlockN, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+  static_assert(kColO + NQ * D <= static_cast<int>(kTmemCols), "tensor memory budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Wait that ignores the abort flag: used to drain copies/MMAs already in flight.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+__device__ int g_status_word = 0;
+
+template <int D, int NQ, int NSTAGE>
+__global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
+  using C = Cfg<D, NQ, NSTAGE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const uint32_t sQ = base;
+  const uint32_t sKV = base + C::kSmemQ;
+  const uint32_t bars = sKV + C::kSmemKV;
+  const uint32_t bar_q_full = bars;
+  auto bar_kv_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto bar_kv_empty = [&](int s) { return bars + 8u * (1 + NSTAGE + s); };
+  auto bar_s_full = [&](int q) { return bars + 8u * (1 + 2 * NSTAGE + q); };
+  auto bar_p_ready = [&](int q) { return bars + 8u * (1 + 2 * NSTAGE + NQ + q); };
+  auto bar_pv_done = [&](int q) { return bars + 8u * (1 + 2 * NSTAGE + 2 * NQ + q); };
+  const uint32_t bar_drain = bars + 8u * (1 + 2 * NSTAGE + 3 * NQ);
+  uint8_t* gmisc = gbase + C::kSmemQ + C::kSmemKV + C::kNumBars * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gmisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit of this CTA -------------------------------------------
+  const int b = blockIdx.z;
+  const int h = blockIdx.y;
+  const int kvh = h / (a.Hq / a.Hkv);
+  const int n_qblocks = gridDim.x;
+  const int qb = n_qblocks - 1 - static_cast<int>(blockIdx.x);  // longest (causal) units first
+  const int q0 = qb * (NQ * kBlockM);
+  int kv_lim = a.Sk;
+  if (a.kv_len) kv_lim = min(kv_lim, max(a.kv_len[b], 0));
+  const bool causal = a.causal || (a.causal_b && a.causal_b[b]);
+  int q_lim = a.Sq;
+  if (a.q_len) q_lim = min(q_lim, max(a.q_len[b], 0));
+  int kv_end = kv_lim;
+  if (causal) kv_end = min(kv_end, q0 + NQ * kBlockM);
+  int n_tiles = (q0 >= q_lim || kv_end <= 0) ? 0 : (kv_end + kBlockN - 1) / kBlockN;
+
+  WaitCtl ctl{abort_flag, &g_status_word, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
+
+  // ---- setup ---------------------------------------------------------------
+  if (warp == C::kProducerWarp && lane == 0) {
+    mbar_init(bar_q_full, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(bar_kv_full(s), 1);
+      mbar_init(bar_kv_empty(s), 1);
+    }
+    for (int q = 0; q < NQ; ++q) {
+      mbar_init(bar_s_full(q), 1);
+      mbar_init(bar_p_ready(q), 128);
+      mbar_init(bar_pv_done(q), 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    prefetch_tmap(&a.tm_q);
+    prefetch_tmap(&a.tm_k);
+    prefetch_tmap(&a.tm_v);
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::kProducerWarp) {
+    // ======================= TMA producer ==================================
+    if (lane == 0 && n_tiles > 0 && !a.debug_skip_producer) {
+      mbar_arrive_expect_tx(bar_q_full, C::kSmemQ);
+      for (int q = 0; q < NQ; ++q)
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sQ + q * C::kTileBytes + c * C::kChunkBytes, &a.tm_q, bar_q_full, c * 64, h,
+                      q0 + q * kBlockM, b);
+      int it = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        bool ok = true;
+        for (int kind = 0; kind < 2; ++kind, ++it) {
+          const int s = it % NSTAGE;
+          const uint32_t ph = (it / NSTAGE) & 1;
+          if (!mbar_wait(bar_kv_empty(s), ph ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_kv_full(s), C::kTileBytes);
+          const CUtensorMap* m = kind == 0 ? &a.tm_k : &a.tm_v;
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(sKV + s * C::kTileBytes + c * C::kChunkBytes, m, bar_kv_full(s), c * 64,
+                        kvh, j * kBlockN, b);
+        }
+        if (!ok) break;
+      }
+      // Drain: every issued copy has landed before the CTA can retire.
+      mbar_wait_drain(bar_q_full, 0, a.wait_limit_ns);
+      const int first = it > NSTAGE ? it - NSTAGE : 0;
+      for (int i = first; i < it; ++i)
+        mbar_wait_drain(bar_kv_full(i % NSTAGE), (i / NSTAGE) & 1, a.wait_limit_ns);
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ======================= MMA issuer ====================================
+    if (lane == 0 && n_tiles > 0) {
+      bool ok = mbar_wait(bar_q_full, 0, ctl);
+      tc_fence_after();
+      int it = 0;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        // S_q = Q_q K_j^T
+        {
+          const int s = it % NSTAGE;
+          const uint32_t ph = (it / NSTAGE) & 1;
+          ++it;
+          if (!(ok = mbar_wait(bar_kv_full(s), ph, ctl))) break;
+          tc_fence_after();
+          for (int q = 0; q < NQ; ++q) {
+            if (j > 0) {
+              if (!(ok = mbar_wait(bar_pv_done(q), (j - 1) & 1, ctl))) break;
+              tc_fence_after();
+            }
+            const uint32_t qa = sQ + q * C::kTileBytes;
+            const uint32_t kb = sKV + s * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+              mma_ss(tmem + q * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                     C::kIdescQK, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(bar_s_full(q));
+          }
+          if (!ok) break;
+          tc_commit(bar_kv_empty(s));
+        }
+        // O_q += P_q V_j
+        {
+          const int s = it % NSTAGE;
+          const uint32_t ph = (it / NSTAGE) & 1;
+          ++it;
+          if (!(ok = mbar_wait(bar_kv_full(s), ph, ctl))) break;
+          tc_fence_after();
+          const uint32_t vb = sKV + s * C::kTileBytes;
+          for (int q = 0; q < NQ; ++q) {
+            if (!(ok = mbar_wait(bar_p_ready(q), j & 1, ctl))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk) {
+              mma_ts(tmem + C::kColO + q * D, tmem + q * 128 + kk * 8,
+                     sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), C::kIdescPV,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(bar_pv_done(q));
+          }
+          if (!ok) break;
+          tc_commit(bar_kv_empty(s));
+        }
+      }
+      // Drain every MMA issued by this thread before tensor memory is freed.
+      tc_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0, a.wait_limit_ns);
+    }
+  } else {
+    // ======================= softmax / correction / epilogue ===============
+    const int q = warp >> 2;         // query tile of this warpgroup
+    const int wq = warp & 3;         // lane quarter of tensor memory
+    const int t = wq * 32 + lane;    // row within the tile
+    const int row = q0 + q * kBlockM + t;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + q * 128;
+    const uint32_t tO = tmem + lane_off + C::kColO + q * D;
+    const float sl = a.scale_log2;
+    const int64_t bit_words = (a.Sk + 31) / 32;
+    float m_ref = -INFINITY;  // running max in scaled (log2) units
+    float l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = mbar_wait(bar_s_full(q), j & 1, ctl);
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+      float s[kBlockN];
+#pragma unroll
+      for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      const int kbase = j * kBlockN;
+      const bool need_mask = (kbase + kBlockN > kv_lim) ||
+                             (causal && kbase + kBlockN - 1 > q0 + q * kBlockM) || a.bits;
+      if (need_mask) {
+        int lim = kv_lim - kbase;
+        if (causal) lim = min(lim, row + 1 - kbase);
+        uint32_t wbits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+        if (a.bits && row < a.Sq) {
+          const uint32_t* br = a.bits + (static_cast<int64_t>(b) * a.Sq + row) * bit_words;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int64_t wi = kbase / 32 + w;
+            wbits[w] = wi < bit_words ? br[wi] : 0u;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c) {
+          const bool allowed = (c < lim) && ((wbits[c >> 5] >> (c & 31)) & 1u);
+          s[c] = allowed ? s[c] : -INFINITY;
+        }
+      }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kBlockN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float mt_s = mt * sl;
+      const bool grow = mt_s > m_ref + kRescaleThreshold;
+      float alpha = 1.0f;
+      if (grow) {
+        alpha = ex2(m_ref - mt_s);  // m_ref = -inf gives 0
+        l *= alpha;
+        m_ref = mt_s;
+      }
+      if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
+        // O_q += P V of the previous tile has completed before this tile's
+        // S_q was issued; the wait below returns at once and is kept as a guard.
+        ok = mbar_wait(bar_pv_done(q), (j - 1) & 1, ctl);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+        tmem_st_wait();
+      }
+      const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t p[2][32];
+#pragma unroll
+      for (int c = 0; c < kBlockN; c += 2) {
+        const float p0 = ex2(fmaf(s[c], sl, -mu));
+        const float p1 = ex2(fmaf(s[c + 1], sl, -mu));
+        ls[(c >> 1) & 3] += p0 + p1;
+        p[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_st32(tS, p[0]);
+      tmem_st32(tS + 32, p[1]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_p_ready(q));
+    }
+    // ---- epilogue: O / l -> bf16 ------------------------------------------
+    if (ok && n_tiles > 0) {
+      ok = mbar_wait(bar_pv_done(q), (n_tiles - 1) & 1, ctl);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      tc_fence_after();
+    }
+    if (ok) {
+      const bool live_row = row < a.Sq;
+      const bool zero_row = row >= q_lim || n_tiles == 0 || !(l > 0.0f);
+      const float inv = zero_row ? 0.0f : 1.0f / l;
+      uint16_t* orow = a.o + ((static_cast<int64_t>(b) * a.Sq + row) * a.Hq + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+        }
+        if (live_row) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              f[e] = zero_row ? 0.0f : __uint_as_float(o[v * 8 + e]) * inv;
+            dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, int NQ, int NSTAGE>
+cudaError_t launch_cfg(const AttnArgs& a, cudaStream_t stream) {
+  using C = Cfg<D, NQ, NSTAGE>;
+  auto kern = attn_fwd_kernel<D, NQ, NSTAGE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int rows_per_cta = NQ * kBlockM;
+  dim3 grid((a.Sq + rows_per_cta - 1) / rows_per_cta, a.Hq, a.B);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Reads and clears the current device's status word (synchronous copies).
+int read_and_clear_status(int* value) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return 1;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return 1;
+  }
+  *value = v;
+  return 0;
+}
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
+  switch (a.D) {
+    case 64: return launch_cfg<64, 2, 8>(a, stream);
+    case 128: return launch_cfg<128, 2, 4>(a, stream);
+    case 256: return launch_cfg<256, 1, 2>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace h3
