@@ -1,0 +1,373 @@
+"""Benchmark of the H3 attention step on GB300.
+
+One step = the whole hot path over one batch of synthetic input: fused Q/K
+RMSNorm + bf16 boundary + partial RoPE (in place) and dense prefill
+attention, both through libh3attn's C ABI.  Default workload: long video
+self-attention, B=1, S=32760, H=24, D=128 (the shape the headline attention
+throughput is quoted on), inputs drawn by h3inputs (seed 0).
+
+Prints one JSON line (rank 0).  `value` = attention FLOP (4*B*Sq*Sk*Hq*D)
+per step / device time per step, inputs resident in HBM (q, k, v: 603 MB,
+larger than the 129 MB L2, so no flush is needed between steps).  `e2e` =
+the same metric when every step also copies q, k, v from pinned host memory
+and reads o back.  `--impl reference` times the CPU oracle on the host
+cores instead (bounded row samples of the same workload).
+
+Multi-GPU: one process per GPU (torchrun); each rank runs its own replica of
+the workload (independent problems, no data-path collective); a barrier and
+a max-over-ranks of the timings are the only communication.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s & % of GB300 BF16 peak at S=32k,H=24,D=128; QK-norm+RoPE GB/s"
+WORKLOAD = "long_video_h24"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _workload_numbers(wl):
+    flops = 4.0 * wl.B * wl.Sq * wl.Sk * wl.Hq * wl.D
+    rows_q = wl.B * wl.Sq * wl.Hq
+    rows_k = 0 if wl.cross else wl.B * wl.Sk * wl.Hkv
+    half = wl.rotary_dim // 2
+    norm_bytes = 2.0 * (rows_q + rows_k) * wl.D * 2 + 2.0 * max(wl.Sq, wl.Sk) * half * 4 + 2.0 * wl.D * 4
+    return flops, norm_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="h3clk", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import h3inputs as gen
+    import video_dit_dense_gb300 as h3
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    h3.build()
+    h3.load()
+    wl = gen.WORKLOADS[args.workload]
+    inp = gen.make_inputs(wl, seed=args.seed + rank)
+    flops, norm_bytes = _workload_numbers(wl)
+    peaks = _peaks()
+
+    def pinned(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    hq, hk, hv = pinned(inp.q), pinned(inp.k), pinned(inp.v)
+    q, k, v = hq.cuda(), hk.cuda(), hv.cuda()
+    o = torch.empty_like(q)
+    ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    wq, wk = torch.from_numpy(inp.wq).cuda(), torch.from_numpy(inp.wk).cuda()
+    cos, sin = torch.from_numpy(inp.cos).cuda(), torch.from_numpy(inp.sin).cuda()
+    kn = None if wl.cross else k
+    wkn = None if wl.cross else wk
+    stream = torch.cuda.current_stream()
+
+    def step():
+        h3.h3attn_qk_norm_rope(q, kn, wq, wkn, cos, sin, wl.rotary_dim, wl.eps, stream)
+        h3.h3attn_prefill(q, k, v, o, wl.scale, None, False, stream)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timing --------------------------------------------
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        h3.h3attn_qk_norm_rope(q, kn, wq, wkn, cos, sin, wl.rotary_dim, wl.eps, stream)
+        ev[i][1].record(stream)
+        h3.h3attn_prefill(q, k, v, o, wl.scale, None, False, stream)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    st = h3.h3attn_check_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {h3.h3attn_status_string(st)}")
+    total_ms = t_start.elapsed_time(t_end)
+    norm_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+
+    # ---- end to end through the public API, host buffers -------------------
+    for _ in range(max(1, args.warmup // 2)):
+        q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    times = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
+    if ws > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = times.tolist()
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+
+    ms_per_step = total_ms / args.steps
+    value = ws * flops * args.steps / (total_ms * 1e-3) / 1e12
+    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+    norm_gbs = norm_bytes / (norm_ms * 1e-3) / 1e9
+    traffic = _profiled_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (h3inputs seed %d: N(0,1) bf16 + N(0,0.5) per-head offsets on q/k)" % args.seed,
+        "config": {
+            "workload": f"{wl.name}: B={wl.B} Sq={wl.Sq} Sk={wl.Sk} Hq={wl.Hq} Hkv={wl.Hkv} D={wl.D}; "
+                        f"QK-norm + RoPE {wl.rotary_dim}/{wl.D} then dense non-causal attention",
+            "l2": "no flush: inputs larger than L2 (q,k,v %.0f MB > 129 MB)" % (3 * wl.B * wl.Sq * wl.Hq * wl.D * 2 / 1e6),
+            "parallelism": f"replicas x{ws} (independent problems per GPU)",
+        },
+        "clocks": clk,
+        "e2e": {
+            "value": round(ws * flops * args.steps / (e2e_ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
+            "d2h_bytes_per_step": int(ho.numel() * 2),
+            "ms_per_step": round(e2e_ms / args.steps, 4),
+        },
+        "gpu_launches": 2 * args.steps,
+        "roofline": {
+            "kernel": "attn_fwd_kernel<128,2,4>",
+            "bound": "tensor",
+            "achieved": round(attn_tflops, 2),
+            "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": round(attn_tflops / peaks["bf16_tflops"], 4),
+            "frac_of_sustained": round(attn_tflops / peaks["bf16_tflops_sustained"], 4),
+            "peak_source": peaks["source"] + " burst bf16 (MEASURED_PEAKS.json)",
+            "traffic": traffic.get("attn"),
+            "ms_per_launch": round(attn_ms, 4),
+        },
+        "norm_rope": {
+            "kernel": "qk_norm_rope_kernel<128>",
+            "bound": "hbm",
+            "achieved": round(norm_gbs, 1),
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": round(norm_gbs / peaks["hbm_gbs"], 4),
+            "frac_of_8tbs": round(norm_gbs / 8000.0, 4),
+            "algorithmic_bytes": int(norm_bytes),
+            "traffic": traffic.get("norm"),
+            "ms_per_launch": round(norm_ms, 4),
+        },
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def _profiled_traffic():
+    """DRAM bytes per launch recorded from an ncu capture of the current kernels, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {}
+
+
+def cpu_baseline(wl, inp, seconds):
+    """The oracle as it stands, on the host cores, on a bounded row sample."""
+    import numpy as np
+
+    import oracle
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    # norm/RoPE oracle (fp64) on the q and k of one slice of tokens
+    t0 = time.perf_counter()
+    n_tok = min(wl.Sq, 2048)
+    oracle.qk_norm_rope_f64(np.ascontiguousarray(inp.q[:, :n_tok]), inp.wq, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+    t_norm = time.perf_counter() - t0
+    # attention oracle on sampled rows, growing the sample until ~`seconds`
+    n = 8
+    done_rows, t_att = 0, 0.0
+    while t_att < seconds:
+        ids = np.sort(rng.choice(wl.B * wl.Sq * wl.Hq, size=n, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.attention_f64(inp.q, inp.k, inp.v, wl.scale, row_ids=ids)
+        t_att += time.perf_counter() - t0
+        done_rows += n
+        n = min(n * 2, 4096)
+    flops_per_row = 4.0 * wl.Sk * wl.D
+    return {"value": round(done_rows * flops_per_row / t_att / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{done_rows} attention rows of {wl.name} (fp64, all {wl.Sk} keys each) in {t_att:.1f} s; "
+                      f"norm/RoPE fp64 on {n_tok * wl.Hq} q rows in {t_norm:.2f} s",
+            "norm_rope_gbs": round(2.0 * n_tok * wl.Hq * wl.D * 2 / t_norm / 1e9, 3)}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle as it stands on the host cores."""
+    import numpy as np
+
+    import h3inputs as gen
+    import oracle
+
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    wl = gen.WORKLOADS[args.workload]
+    inp = gen.make_inputs(wl, seed=args.seed)
+    flops_per_row = 4.0 * wl.Sk * wl.D
+    rows_per_step = args.ref_rows
+    rng = np.random.default_rng(0)
+
+    def one_step():
+        ids = np.sort(rng.choice(wl.B * wl.Sq * wl.Hq, size=rows_per_step, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.qk_norm_rope_f64(np.ascontiguousarray(inp.q[:, :256]), inp.wq, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+        oracle.attention_f64(inp.q, inp.k, inp.v, wl.scale, row_ids=ids)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one_step()
+    t = sum(one_step() for _ in range(args.steps))
+    value = rows_per_step * args.steps * flops_per_row / t / 1e12
+    cores = os.cpu_count() or 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: B={wl.B} Sq={wl.Sq} Sk={wl.Sk} Hq={wl.Hq} Hkv={wl.Hkv} D={wl.D}; "
+                               f"CPU oracle, {rows_per_step} sampled attention rows per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} attention rows (all {wl.Sk} keys) + norm/RoPE of 256 tokens per step"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-baseline", dest="cpu_baseline", action="store_true", default=True)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

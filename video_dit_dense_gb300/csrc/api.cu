@@ -116,6 +116,7 @@ h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const flo
   const int64_t rows_q = static_cast<int64_t>(B) * S * Hq;
   const int64_t rows_k = static_cast<int64_t>(B) * S * Hkv;
   if (rows_q + rows_k == 0) return H3ATTN_OK;
+  if (rows_q + rows_k >= (1LL << 31)) return H3ATTN_ERR_INVALID_ARG;
   if ((q && !aligned16(q)) || (k && !aligned16(k)) || (wq && !aligned16(wq)) ||
       (wk && !aligned16(wk)) || (cos && !aligned16(cos)) || (sin && !aligned16(sin)))
     return H3ATTN_ERR_MISALIGNED;
@@ -129,11 +130,11 @@ h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const flo
   a.wk = wk;
   a.cos = cos;
   a.sin = sin;
-  a.rows_q = rows_q;
-  a.rows_k = rows_k;
-  a.S = S;
-  a.Hq = Hq > 0 ? Hq : 1;
-  a.Hkv = Hkv > 0 ? Hkv : 1;
+  a.rows_q = static_cast<uint32_t>(rows_q);
+  a.rows_k = static_cast<uint32_t>(rows_k);
+  a.div_hq = h3::make_fastdiv(static_cast<uint32_t>(Hq > 0 ? Hq : 1));
+  a.div_hkv = h3::make_fastdiv(static_cast<uint32_t>(Hkv > 0 ? Hkv : 1));
+  a.div_s = h3::make_fastdiv(static_cast<uint32_t>(S > 0 ? S : 1));
   a.D = D;
   a.rotary_dim = rotary_dim;
   a.eps = eps;

@@ -54,9 +54,21 @@ struct Cfg {
   static constexpr int kSmemKV = NSTAGE * kTileBytes;
   static constexpr int kNumBars = 1 + 2 * NSTAGE + 3 * NQ + 1;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kSmemQ + kSmemKV + kNumBars * 8 + 16;
-  static constexpr int kThreads = NQ * 128 + 64;
+  // NQ softmax warpgroups + one control warpgroup (producer, MMA issuer, two idle warps)
+  static constexpr int kThreads = NQ * 128 + 128;
   static constexpr int kProducerWarp = NQ * 4;
   static constexpr int kMmaWarp = NQ * 4 + 1;
+  // Register split: launch budget kThreads * floor(65536 / kThreads) (rounded to 8);
+  // the control warpgroup drops to kCtlRegs, softmax warpgroups rise to kSoftRegs.
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
+  static constexpr int kCtlRegs = 96;
+  static constexpr int kSoftRegs =
+      ((kThreads * kLaunchRegs - 128 * kCtlRegs) / (NQ * 128)) / 8 * 8 > 232
+          ? 232
+          : ((kThreads * kLaunchRegs - 128 * kCtlRegs) / (NQ * 128)) / 8 * 8;
+  static_assert(NQ * 128 * kSoftRegs + 128 * kCtlRegs <= kThreads * kLaunchRegs, "register split");
+  // Only needed when the launch budget per thread is below what softmax wants.
+  static constexpr bool kRebalance = kLaunchRegs < 200;
   static constexpr int kColO = NQ * 128;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kBlockN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
@@ -158,7 +170,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == C::kProducerWarp) {
+  if (warp >= NQ * 4) {
+   if constexpr (C::kRebalance) regs_dec<C::kCtlRegs>();
+   if (warp == C::kProducerWarp) {
     // ======================= TMA producer ==================================
     if (lane == 0 && n_tiles > 0 && !a.debug_skip_producer) {
       mbar_arrive_expect_tx(bar_q_full, C::kSmemQ);
@@ -249,7 +263,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
       tc_commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, a.wait_limit_ns);
     }
+   }
   } else {
+    if constexpr (C::kRebalance) regs_inc<C::kSoftRegs>();
     // ======================= softmax / correction / epilogue ===============
     const int q = warp >> 2;         // query tile of this warpgroup
     const int wq = warp & 3;         // lane quarter of tensor memory
@@ -300,13 +316,16 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
           s[c] = allowed ? s[c] : -INFINITY;
         }
       }
+      // row max: 3-input max in 8 independent chains
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-      for (int c = 8; c < kBlockN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 16; c < kBlockN; c += 16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+      }
+      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
       const float mt_s = mt * sl;
       const bool grow = mt_s > m_ref + kRescaleThreshold;
       float alpha = 1.0f;
@@ -336,16 +355,20 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
         tmem_st_wait();
       }
       const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = exp2(s * scale*log2e - m): packed FMA, ex2, packed row-sum
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t p[2][32];
 #pragma unroll
       for (int c = 0; c < kBlockN; c += 2) {
-        const float p0 = ex2(fmaf(s[c], sl, -mu));
-        const float p1 = ex2(fmaf(s[c + 1], sl, -mu));
-        ls[(c >> 1) & 3] += p0 + p1;
+        float t0, t1;
+        ffma2(t0, t1, s[c], s[c + 1], sl, sl, -mu, -mu);
+        const float p0 = ex2(t0);
+        const float p1 = ex2(t1);
+        const int a2 = ((c >> 1) & 3) * 2;
+        fadd2(ls[a2], ls[a2 + 1], ls[a2], ls[a2 + 1], p0, p1);
         p[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tmem_st32(tS, p[0]);
       tmem_st32(tS + 32, p[1]);
       tmem_st_wait();

@@ -14,6 +14,24 @@ namespace h3 {
 int read_and_clear_status(int* value);
 
 // ---- fused Q/K RMSNorm + bf16 boundary + partial RoPE (in place) ----
+// Division of 32-bit unsigned integers by a runtime constant d with one
+// 64x64 multiply-high: q = floor(M * n / 2^64), M = floor((2^64 - 1) / d) + 1,
+// exact for every 32-bit n (Lemire, Kaser and Kurz, "Faster remainder by
+// direct computation", Software: Practice and Experience 49(6), 2019).
+// d == 1 is handled by the caller-visible flag `one`.
+struct FastDiv {
+  uint64_t M;
+  uint32_t d;
+  uint32_t one;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  f.one = d == 1 ? 1u : 0u;
+  f.M = d == 1 ? 0ull : (~0ull) / d + 1ull;
+  return f;
+}
+
 struct NormRopeArgs {
   uint16_t* q;
   uint16_t* k;
@@ -21,9 +39,10 @@ struct NormRopeArgs {
   const float* wk;
   const float* cos;
   const float* sin;
-  int64_t rows_q;  // B * S * Hq
-  int64_t rows_k;  // B * S * Hkv
-  int S, Hq, Hkv, D, rotary_dim;
+  uint32_t rows_q;  // B * S * Hq   (host guarantees rows_q + rows_k < 2^31)
+  uint32_t rows_k;  // B * S * Hkv
+  FastDiv div_hq, div_hkv, div_s;  // row -> token = row / H, position = token % S
+  int D, rotary_dim;
   float eps;
 };
 cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
