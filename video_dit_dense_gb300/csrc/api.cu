@@ -138,6 +138,9 @@ h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const flo
   a.D = D;
   a.rotary_dim = rotary_dim;
   a.eps = eps;
+  a.status = h3::status_word_ptr();
+  if (!a.status) return H3ATTN_ERR_LAUNCH;
+  a.wait_limit_ns = wait_limit_ns();
   cudaError_t e = h3::launch_qk_norm_rope(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_LAUNCH;
 }

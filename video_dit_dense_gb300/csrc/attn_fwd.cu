@@ -98,6 +98,26 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
 
 __device__ int g_status_word = 0;
 
+#ifdef H3ATTN_TRACE
+// Optional pipeline trace (compile with -DH3ATTN_TRACE): clock64 stamps of
+// the first CTA's producer, MMA issuer and softmax threads, per key tile.
+constexpr int kTraceTiles = 512;
+enum TraceEv {
+  kEvProdK, kEvProdV, kEvMmaK, kEvMmaQK0, kEvMmaQK1, kEvMmaV, kEvMmaPV0, kEvMmaPV1,
+  kEvSmS0, kEvSmLd0, kEvSmExp0, kEvSmArr0, kEvSmS1, kEvSmLd1, kEvSmExp1, kEvSmArr1, kNumEv
+};
+__device__ unsigned long long g_trace[kNumEv][kTraceTiles];
+#define H3_TRACE(ev, j)                                                                     \
+  do {                                                                                      \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (j) < kTraceTiles)         \
+      g_trace[(ev)][(j)] = clock64();                                                       \
+  } while (0)
+#else
+#define H3_TRACE(ev, j) \
+  do {                  \
+  } while (0)
+#endif
+
 template <int D, int NQ, int NSTAGE>
 __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
@@ -190,6 +210,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
             ok = false;
             break;
           }
+          H3_TRACE(kind == 0 ? kEvProdK : kEvProdV, j);
           mbar_arrive_expect_tx(bar_kv_full(s), C::kTileBytes);
           const CUtensorMap* m = kind == 0 ? &a.tm_k : &a.tm_v;
           for (int c = 0; c < C::kChunks; ++c)
@@ -217,12 +238,14 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
           const uint32_t ph = (it / NSTAGE) & 1;
           ++it;
           if (!(ok = mbar_wait(bar_kv_full(s), ph, ctl))) break;
+          H3_TRACE(kEvMmaK, j);
           tc_fence_after();
           for (int q = 0; q < NQ; ++q) {
             if (j > 0) {
               if (!(ok = mbar_wait(bar_pv_done(q), (j - 1) & 1, ctl))) break;
               tc_fence_after();
             }
+            H3_TRACE(kEvMmaQK0 + q, j);
             const uint32_t qa = sQ + q * C::kTileBytes;
             const uint32_t kb = sKV + s * C::kTileBytes;
 #pragma unroll
@@ -242,10 +265,12 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
           const uint32_t ph = (it / NSTAGE) & 1;
           ++it;
           if (!(ok = mbar_wait(bar_kv_full(s), ph, ctl))) break;
+          H3_TRACE(kEvMmaV, j);
           tc_fence_after();
           const uint32_t vb = sKV + s * C::kTileBytes;
           for (int q = 0; q < NQ; ++q) {
             if (!(ok = mbar_wait(bar_p_ready(q), j & 1, ctl))) break;
+            H3_TRACE(kEvMmaPV0 + q, j);
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kBlockN / 16; ++kk) {
@@ -281,6 +306,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       ok = mbar_wait(bar_s_full(q), j & 1, ctl);
+      if (t == 0) H3_TRACE(kEvSmS0 + 4 * q, j);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
         break;
@@ -291,6 +317,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+      if (t == 0) H3_TRACE(kEvSmLd0 + 4 * q, j);
       float s[kBlockN];
 #pragma unroll
       for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -369,11 +396,13 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
         p[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
       }
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      if (t == 0) H3_TRACE(kEvSmExp0 + 4 * q, j);
       tmem_st32(tS, p[0]);
       tmem_st32(tS + 32, p[1]);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p_ready(q));
+      if (t == 0) H3_TRACE(kEvSmArr0 + 4 * q, j);
     }
     // ---- epilogue: O / l -> bf16 ------------------------------------------
     if (ok && n_tiles > 0) {
@@ -430,6 +459,26 @@ cudaError_t launch_cfg(const AttnArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+#ifdef H3ATTN_TRACE
+extern "C" int h3attn_trace_read(unsigned long long* dst, int n) {
+  const int total = kNumEv * kTraceTiles;
+  if (n < total) return -1;
+  return cudaMemcpyFromSymbol(dst, g_trace, sizeof(unsigned long long) * total) == cudaSuccess ? total : -2;
+}
+#endif
+
+int* status_word_ptr() {
+  static int* cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    int* p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status_word) != cudaSuccess) return nullptr;
+    cache[dev] = p;
+  }
+  return cache[dev];
+}
 
 // Reads and clears the current device's status word (synchronous copies).
 int read_and_clear_status(int* value) {

@@ -12,6 +12,8 @@ namespace h3 {
 
 // Reads and clears the current device's status word (see h3attn_check_device_status).
 int read_and_clear_status(int* value);
+// Device address of the current device's status word (nullptr on failure).
+int* status_word_ptr();
 
 // ---- fused Q/K RMSNorm + bf16 boundary + partial RoPE (in place) ----
 // Division of 32-bit unsigned integers by a runtime constant d with one
@@ -44,6 +46,8 @@ struct NormRopeArgs {
   FastDiv div_hq, div_hkv, div_s;  // row -> token = row / H, position = token % S
   int D, rotary_dim;
   float eps;
+  int* status;             // device status word (bounded-wait timeouts)
+  uint64_t wait_limit_ns;  // per-wait limit
 };
 cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
 

@@ -8,11 +8,15 @@
 // RoPE fused in one kernel).  Memory-bound: every row is read once and
 // written once.
 //
-// Layout of the work: a row is one (token, head) vector of D bf16 channels
-// (D*2 bytes).  D/8 consecutive lanes own a row, each holding 8 channels in
-// one 16-byte load, so a warp covers 32*8/D rows per instruction and every
-// load/store instruction of a warp touches 512 contiguous bytes.  Each warp
-// keeps UNROLL such loads in flight before it computes.
+// Layout of the work: a row is one (token, head) vector of D bf16 channels.
+// q rows ([B*S*Hq, D]) and k rows ([B*S*Hkv, D]) are contiguous, so the work
+// is a list of 16 KiB chunks of whole rows.  A persistent grid walks the
+// chunk list; in each CTA one producer warp streams chunks into a ring of
+// shared-memory stages with 1-D bulk copies (completion on an mbarrier), and
+// eight compute warps read rows from shared memory, compute, and store the
+// results straight to global memory.  D/8 consecutive lanes own a row, each
+// holding 8 channels (one 16-byte access), so a warp covers 256/D... rows
+// per access and every access of a warp is 512 contiguous bytes.
 //
 // Arithmetic (float32, fixed order -- reproducible bit for bit):
 //   lane partial: acc = fma(x, x, acc) over its 8 channels in order, from 0;
@@ -20,17 +24,30 @@
 //   ms = acc * (1/D); r = 1 / sqrt(ms + eps), correctly rounded;
 //   n = bf16((x * r) * w); rotation with y_i = fma(a, c, -(b*s)),
 //   y_{i+h} = fma(b, c, a*s); store bf16(y) (round to nearest even).
-// Explicit __f*_rn intrinsics keep the compiler from contracting or
-// reassociating any of it.
+// Explicit round-to-nearest intrinsics and packed f32x2 instructions (each
+// lane rounded once) keep the compiler from contracting or reassociating.
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace h3 {
 namespace {
 
-constexpr int kNormThreads = 256;
-constexpr int kNormUnroll = 4;  // rows per lane slot in flight; also the rows sharing one sqrt/div pass
+constexpr int kComputeWarps = 8;
+constexpr int kStages = 4;
+constexpr int kNormThreads = (kComputeWarps + 1) * 32;  // + one producer warp
+constexpr int kChunkBytes = 16384;
+constexpr int kUnroll = 4;  // rows per lane slot per chunk; also rows sharing one sqrt/div pass
+
+template <int D>
+struct NormCfg {
+  static constexpr int LPR = D / 8;                         // lanes per row
+  static constexpr int RPW = 32 / LPR;                      // rows per warp per access
+  static constexpr int kRows = kChunkBytes / (D * 2);       // rows per chunk
+  static_assert(kRows == kComputeWarps * RPW * kUnroll, "chunk = compute warps x rows per warp");
+  static constexpr int kSmem = kStages * kChunkBytes + 2 * kStages * 8 + 16;
+};
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -43,14 +60,70 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
   return f.one ? n : static_cast<uint32_t>(__umul64hi(f.M, static_cast<uint64_t>(n)));
 }
 
+__device__ __forceinline__ void chunk_of(const NormRopeArgs& a, uint32_t c, uint32_t rows_per_chunk,
+                                         uint32_t n_q_chunks, bool& is_q, uint32_t& row0, uint32_t& nrows) {
+  is_q = c < n_q_chunks;
+  const uint32_t cc = is_q ? c : c - n_q_chunks;
+  const uint32_t limit = is_q ? a.rows_q : a.rows_k;
+  row0 = cc * rows_per_chunk;
+  nrows = min(rows_per_chunk, limit - row0);
+}
+
 template <int D>
-__global__ void __launch_bounds__(kNormThreads) qk_norm_rope_kernel(const __grid_constant__ NormRopeArgs a) {
-  constexpr int LPR = D / 8;     // lanes per row
-  constexpr int RPW = 32 / LPR;  // rows per warp per load instruction
-  constexpr int U = kNormUnroll;
+__global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __grid_constant__ NormRopeArgs a) {
+  using C = NormCfg<D>;
+  constexpr int LPR = C::LPR, RPW = C::RPW, U = kUnroll;
   constexpr float kInvD = 1.0f / static_cast<float>(D);
   static_assert(LPR >= U, "each row needs a lane per unrolled row for the shared sqrt/div pass");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kStages * kChunkBytes;
+  auto bar_full = [&](int st) { return bars + 8u * st; };
+  auto bar_empty = [&](int st) { return bars + 8u * (kStages + st); };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kStages * kChunkBytes + 2 * kStages * 8);
+  WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
+
+  const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(bar_full(st), 1);
+      mbar_init(bar_empty(st), kComputeWarps);
+    }
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const uint32_t n_q_chunks = (a.rows_q + C::kRows - 1) / C::kRows;
+  const uint32_t n_chunks = n_q_chunks + (a.rows_k + C::kRows - 1) / C::kRows;
+
+  if (warp == kComputeWarps) {
+    // ---------------- producer: chunk -> shared-memory stage ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (uint32_t c = blockIdx.x; c < n_chunks; c += gridDim.x, ++it) {
+        const int st = it % kStages;
+        if (!mbar_wait(bar_empty(st), ((it / kStages) & 1) ^ 1u, ctl)) break;
+        bool is_q;
+        uint32_t row0, nrows;
+        chunk_of(a, c, C::kRows, n_q_chunks, is_q, row0, nrows);
+        const uint16_t* src = (is_q ? a.q : a.k) + static_cast<size_t>(row0) * D;
+        mbar_arrive_expect_tx(bar_full(st), nrows * D * 2);
+        bulk_load(sbase + st * kChunkBytes, src, nrows * D * 2, bar_full(st));
+      }
+      // every issued copy has landed before the CTA retires
+      const uint32_t first = it > kStages ? it - kStages : 0;
+      for (uint32_t i = first; i < it; ++i) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar_full(i % kStages), (i / kStages) & 1))
+          if (globaltimer_ns() - t0 > a.wait_limit_ns) break;
+      }
+    }
+    return;
+  }
+
+  // ---------------- compute warps ----------------
   const uint32_t lr = lane % LPR;  // lane within its row
   const uint32_t slot = lane / LPR;
   const uint32_t row_lane0 = lane - lr;
@@ -59,25 +132,30 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_rope_kernel(const __grid
   const bool rotating = lr < 2 * hl;
   // Rotation partner: lanes [0, hl) pair with [hl, 2hl) of the same row.
   const uint32_t partner = lr < hl ? lane + hl : (rotating ? lane - hl : lane);
-  const uint32_t ti = rotating ? (lr < hl ? lr : lr - hl) * 8 : 0;  // table column of channel 0 of this lane
-  const uint32_t neg = lr < hl ? 0x80000000u : 0u;                 // y_i takes -(b*s), y_{i+h} takes +(a*s)
-  const uint32_t total = a.rows_q + a.rows_k;
-  const uint32_t warp = (blockIdx.x * kNormThreads + threadIdx.x) >> 5;
-  const uint32_t nwarps = (gridDim.x * kNormThreads) >> 5;
+  const uint32_t ti = rotating ? (lr < hl ? lr : lr - hl) * 8 : 0;  // table column of this lane's channel 0
+  const uint32_t neg = lr < hl ? 0x80000000u : 0u;  // y_i takes -(b*s), y_{i+h} takes +(a*s)
 
-  for (uint32_t base = warp * (RPW * U); base < total; base += nwarps * (RPW * U)) {
+  uint32_t it = 0;
+  for (uint32_t c = blockIdx.x; c < n_chunks; c += gridDim.x, ++it) {
+    const int st = it % kStages;
+    const bool ok = mbar_wait(bar_full(st), (it / kStages) & 1, ctl);
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    bool is_q;
+    uint32_t row0, nrows;
+    chunk_of(a, c, C::kRows, n_q_chunks, is_q, row0, nrows);
+    const uint8_t* stage = smem + st * kChunkBytes;
+
     uint4 xv[U];
-    uint32_t row[U];
+    uint32_t lrow[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      row[u] = base + u * RPW + slot;
-      xv[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (row[u] < total) {
-        const uint16_t* p = row[u] < a.rows_q ? a.q + static_cast<size_t>(row[u]) * D
-                                              : a.k + static_cast<size_t>(row[u] - a.rows_q) * D;
-        xv[u] = *reinterpret_cast<const uint4*>(p + lr * 8);
-      }
+      lrow[u] = (warp * U + u) * RPW + slot;
+      xv[u] = lrow[u] < nrows ? *reinterpret_cast<const uint4*>(stage + lrow[u] * (D * 2) + lr * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty(st));  // the stage may be refilled
+
     // Sum of squares: lane partial in channel order, then the butterfly.
     float acc[U];
 #pragma unroll
@@ -108,63 +186,79 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_rope_kernel(const __grid
 #pragma unroll
     for (int u = 0; u < U; ++u) rinv[u] = __shfl_sync(0xFFFFFFFFu, r_mine, row_lane0 + u);
 
+    const float* wp = (is_q ? a.wq : a.wk) + lr * 8;
+    const float4 w0 = __ldg(reinterpret_cast<const float4*>(wp));
+    const float4 w1 = __ldg(reinterpret_cast<const float4*>(wp + 4));
+    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const FastDiv& dh = is_q ? a.div_hq : a.div_hkv;
+    uint16_t* gbase = is_q ? a.q : a.k;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const bool is_q = row[u] < a.rows_q;
-      const uint32_t r = is_q ? row[u] : row[u] - a.rows_q;
-      const float* wp = (is_q ? a.wq : a.wk) + lr * 8;
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(wp));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(wp + 4));
-      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
       const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
       // boundary values n^ = bf16((x * r) * w), kept as bf16 pairs
       uint32_t nb[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float n0 = __fmul_rn(__fmul_rn(bf16lo(xw[e]), rinv[u]), wv[2 * e]);
-        const float n1 = __fmul_rn(__fmul_rn(bf16hi(xw[e]), rinv[u]), wv[2 * e + 1]);
+        float t0, t1, n0, n1;
+        fmul2(t0, t1, bf16lo(xw[e]), bf16hi(xw[e]), rinv[u], rinv[u]);
+        fmul2(n0, n1, t0, t1, wv[2 * e], wv[2 * e + 1]);
         nb[e] = pack_bf16(n0, n1);
       }
       uint32_t pb[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) pb[e] = __shfl_sync(0xFFFFFFFFu, nb[e], partner);
-      if (row[u] >= total) continue;
+      if (lrow[u] >= nrows) continue;
+      const uint32_t r = row0 + lrow[u];
       uint32_t ob[4] = {nb[0], nb[1], nb[2], nb[3]};
       if (rotating) {
-        const uint32_t tok = fdiv(r, is_q ? a.div_hq : a.div_hkv);
+        const uint32_t tok = fdiv(r, dh);
         const uint32_t pos = tok - fdiv(tok, a.div_s) * a.div_s.d;
         const float* ct = a.cos + static_cast<size_t>(pos) * half + ti;
-        const float* st = a.sin + static_cast<size_t>(pos) * half + ti;
+        const float* stb = a.sin + static_cast<size_t>(pos) * half + ti;
         const float4 c0 = __ldg(reinterpret_cast<const float4*>(ct));
         const float4 c1 = __ldg(reinterpret_cast<const float4*>(ct + 4));
-        const float4 s0 = __ldg(reinterpret_cast<const float4*>(st));
-        const float4 s1 = __ldg(reinterpret_cast<const float4*>(st + 4));
+        const float4 s0 = __ldg(reinterpret_cast<const float4*>(stb));
+        const float4 s1 = __ldg(reinterpret_cast<const float4*>(stb + 4));
         const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        // sine with this lane's sign folded in: (-s) * b == -(b * s) exactly
+        const float sv[8] = {__uint_as_float(__float_as_uint(s0.x) ^ neg), __uint_as_float(__float_as_uint(s0.y) ^ neg),
+                             __uint_as_float(__float_as_uint(s0.z) ^ neg), __uint_as_float(__float_as_uint(s0.w) ^ neg),
+                             __uint_as_float(__float_as_uint(s1.x) ^ neg), __uint_as_float(__float_as_uint(s1.y) ^ neg),
+                             __uint_as_float(__float_as_uint(s1.z) ^ neg), __uint_as_float(__float_as_uint(s1.w) ^ neg)};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float own0 = bf16lo(nb[e]), own1 = bf16hi(nb[e]);
-          const float oth0 = bf16lo(pb[e]), oth1 = bf16hi(pb[e]);
-          const float t0 = __uint_as_float(__float_as_uint(__fmul_rn(oth0, sv[2 * e])) ^ neg);
-          const float t1 = __uint_as_float(__float_as_uint(__fmul_rn(oth1, sv[2 * e + 1])) ^ neg);
-          ob[e] = pack_bf16(__fmaf_rn(own0, cv[2 * e], t0), __fmaf_rn(own1, cv[2 * e + 1], t1));
+          float t0, t1, y0, y1;
+          fmul2(t0, t1, bf16lo(pb[e]), bf16hi(pb[e]), sv[2 * e], sv[2 * e + 1]);
+          ffma2(y0, y1, bf16lo(nb[e]), bf16hi(nb[e]), cv[2 * e], cv[2 * e + 1], t0, t1);
+          ob[e] = pack_bf16(y0, y1);
         }
       }
-      uint16_t* p = is_q ? a.q + static_cast<size_t>(r) * D : a.k + static_cast<size_t>(r) * D;
-      *reinterpret_cast<uint4*>(p + lr * 8) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+      *reinterpret_cast<uint4*>(gbase + static_cast<size_t>(r) * D + lr * 8) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
     }
   }
 }
 
 template <int D>
 cudaError_t launch_d(const NormRopeArgs& a, cudaStream_t stream) {
-  constexpr int RPW = 32 / (D / 8);
-  const int64_t total = static_cast<int64_t>(a.rows_q) + a.rows_k;
-  const int64_t rows_per_block = static_cast<int64_t>(kNormThreads / 32) * RPW * kNormUnroll;
-  int64_t blocks = (total + rows_per_block - 1) / rows_per_block;
-  if (blocks > 65536) blocks = 65536;  // the kernel's grid-stride loop covers the rest
+  using C = NormCfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(qk_norm_rope_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t chunks = (static_cast<int64_t>(a.rows_q) + C::kRows - 1) / C::kRows +
+                         (static_cast<int64_t>(a.rows_k) + C::kRows - 1) / C::kRows;
+  int64_t blocks = static_cast<int64_t>(sms) * 3;  // three resident CTAs per SM
+  if (blocks > chunks) blocks = chunks;
   if (blocks == 0) return cudaSuccess;
-  qk_norm_rope_kernel<D><<<static_cast<unsigned>(blocks), kNormThreads, 0, stream>>>(a);
+  qk_norm_rope_kernel<D><<<static_cast<unsigned>(blocks), kNormThreads, C::kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
