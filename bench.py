@@ -53,6 +53,20 @@ def _dist():
     return ws, rank, local
 
 
+def _allowed_pairs(wl, kv_len, causal_b):
+    """Allowed (query row, key) pairs summed over samples (structured masks)."""
+    total = 0
+    for b in range(wl.B):
+        L = wl.Sk if kv_len is None else max(0, min(wl.Sk, int(kv_len[b])))
+        if causal_b is not None and causal_b[b]:
+            # rows i < L attend i+1 keys, rows i >= L attend L keys
+            m = min(L, wl.Sq)
+            total += m * (m + 1) // 2 + (wl.Sq - m) * L
+        else:
+            total += wl.Sq * L
+    return total
+
+
 def _workload_numbers(wl):
     flops = 4.0 * wl.B * wl.Sq * wl.Sk * wl.Hq * wl.D
     rows_q = wl.B * wl.Sq * wl.Hq
@@ -124,7 +138,10 @@ def run_gpu(args):
     h3.load()
     wl = gen.WORKLOADS[args.workload]
     inp = gen.make_inputs(wl, seed=args.seed + rank)
-    flops, norm_bytes = _workload_numbers(wl)
+    flops_nominal, norm_bytes = _workload_numbers(wl)
+    # algorithmic flops: 4*D*Hq per allowed (row, key) pair; equals the nominal
+    # 4*B*Sq*Sk*Hq*D for unmasked workloads
+    flops = 4.0 * wl.D * wl.Hq * _allowed_pairs(wl, inp.kv_len, inp.causal_b)
     peaks = _peaks()
 
     def pinned(bits):
@@ -134,15 +151,22 @@ def run_gpu(args):
     q, k, v = hq.cuda(), hk.cuda(), hv.cuda()
     o = torch.empty_like(q)
     ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
-    wq, wk = torch.from_numpy(inp.wq).cuda(), torch.from_numpy(inp.wk).cuda()
-    cos, sin = torch.from_numpy(inp.cos).cuda(), torch.from_numpy(inp.sin).cuda()
+    wq = wk = cos = sin = None
+    if wl.norm_rope:
+        wq, wk = torch.from_numpy(inp.wq).cuda(), torch.from_numpy(inp.wk).cuda()
+        cos, sin = torch.from_numpy(inp.cos).cuda(), torch.from_numpy(inp.sin).cuda()
     kn = None if wl.cross else k
     wkn = None if wl.cross else wk
+    mask = None
+    if inp.kv_len is not None or inp.causal_b is not None:
+        mask = h3.Mask(kv_len=None if inp.kv_len is None else torch.from_numpy(inp.kv_len).cuda(),
+                       causal_b=None if inp.causal_b is None else torch.from_numpy(inp.causal_b).cuda())
     stream = torch.cuda.current_stream()
 
     def step():
-        h3.h3attn_qk_norm_rope(q, kn, wq, wkn, cos, sin, wl.rotary_dim, wl.eps, stream)
-        h3.h3attn_prefill(q, k, v, o, wl.scale, None, False, stream)
+        if wl.norm_rope:
+            h3.h3attn_qk_norm_rope(q, kn, wq, wkn, cos, sin, wl.rotary_dim, wl.eps, stream)
+        h3.h3attn_prefill(q, k, v, o, wl.scale, mask, False, stream)
 
     def barrier():
         if ws > 1:
@@ -162,9 +186,10 @@ def run_gpu(args):
     t_start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
-        h3.h3attn_qk_norm_rope(q, kn, wq, wkn, cos, sin, wl.rotary_dim, wl.eps, stream)
+        if wl.norm_rope:
+            h3.h3attn_qk_norm_rope(q, kn, wq, wkn, cos, sin, wl.rotary_dim, wl.eps, stream)
         ev[i][1].record(stream)
-        h3.h3attn_prefill(q, k, v, o, wl.scale, None, False, stream)
+        h3.h3attn_prefill(q, k, v, o, wl.scale, mask, False, stream)
         ev[i][2].record(stream)
     t_end.record(stream)
     barrier()
@@ -205,8 +230,17 @@ def run_gpu(args):
     ms_per_step = total_ms / args.steps
     value = ws * flops * args.steps / (total_ms * 1e-3) / 1e12
     attn_tflops = flops / (attn_ms * 1e-3) / 1e12
-    norm_gbs = norm_bytes / (norm_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic()
+    norm_gbs = norm_bytes / (norm_ms * 1e-3) / 1e9 if wl.norm_rope else None
+    # recorded traffic is for the default workload's launches only
+    traffic = _profiled_traffic() if wl.name == WORKLOAD else {}
+    attn_kernel = {64: "attn_fwd_kernel<64,2,8>", 128: "attn_fwd_kernel<128,2,4>", 256: "attn_fwd_kernel<256,1,2>"}[wl.D]
+    masks = []
+    if inp.kv_len is not None:
+        masks.append("key padding kv_len=%s" % list(map(int, inp.kv_len)))
+    if inp.causal_b is not None:
+        masks.append("causal per sample %s" % list(map(int, inp.causal_b)))
+    what = ("QK-norm + RoPE %d/%d then " % (wl.rotary_dim, wl.D) if wl.norm_rope else "") + \
+        ("cross-attention" if wl.cross else "self-attention") + (" with " + ", ".join(masks) if masks else " (dense, non-causal)")
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -221,8 +255,9 @@ def run_gpu(args):
         "dtype": "bf16",
         "data": "synthetic (h3inputs seed %d: N(0,1) bf16 + N(0,0.5) per-head offsets on q/k)" % args.seed,
         "config": {
-            "workload": f"{wl.name}: B={wl.B} Sq={wl.Sq} Sk={wl.Sk} Hq={wl.Hq} Hkv={wl.Hkv} D={wl.D}; "
-                        f"QK-norm + RoPE {wl.rotary_dim}/{wl.D} then dense non-causal attention",
+            "workload": f"{wl.name}: B={wl.B} Sq={wl.Sq} Sk={wl.Sk} Hq={wl.Hq} Hkv={wl.Hkv} D={wl.D}; {what}",
+            "flops_per_step": flops,
+            "flops_nominal_per_step": flops_nominal,
             "l2": "no flush: inputs larger than L2 (q,k,v %.0f MB > 129 MB)" % (3 * wl.B * wl.Sq * wl.Hq * wl.D * 2 / 1e6),
             "parallelism": f"replicas x{ws} (independent problems per GPU)",
         },
@@ -234,9 +269,9 @@ def run_gpu(args):
             "d2h_bytes_per_step": int(ho.numel() * 2),
             "ms_per_step": round(e2e_ms / args.steps, 4),
         },
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (2 if wl.norm_rope else 1) * args.steps,
         "roofline": {
-            "kernel": "attn_fwd_kernel<128,2,4>",
+            "kernel": attn_kernel,
             "bound": "tensor",
             "achieved": round(attn_tflops, 2),
             "peak": peaks["bf16_tflops"],
@@ -247,8 +282,8 @@ def run_gpu(args):
             "traffic": traffic.get("attn"),
             "ms_per_launch": round(attn_ms, 4),
         },
-        "norm_rope": {
-            "kernel": "qk_norm_rope_kernel<128>",
+        "norm_rope": None if not wl.norm_rope else {
+            "kernel": "qk_norm_rope_kernel<%d>" % wl.D,
             "bound": "hbm",
             "achieved": round(norm_gbs, 1),
             "peak": peaks["hbm_gbs"],
@@ -268,12 +303,25 @@ def run_gpu(args):
 
 
 def _profiled_traffic():
-    """DRAM bytes per launch recorded from an ncu capture of the current kernels, if any."""
+    """DRAM bytes per launch recorded from an ncu capture, per kernel; a kernel
+    whose sources changed since the capture (hash mismatch) reports None."""
+    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(p):
-        with open(p) as f:
-            return json.load(f)
-    return {}
+    out = {}
+    if not os.path.exists(p):
+        return out
+    with open(p) as f:
+        rec = json.load(f)
+    for key in ("attn", "norm"):
+        r = rec.get(key)
+        if not r:
+            continue
+        h = hashlib.sha256()
+        for name in r["sources"]:
+            with open(os.path.join(ROOT, "video_dit_dense_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        out[key] = r["bytes_per_launch"] if h.hexdigest()[:16] == r["source_sha"] else None
+    return out
 
 
 def cpu_baseline(wl, inp, seconds):
