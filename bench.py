@@ -261,7 +261,7 @@ def run_gpu(args):
     norm_gbs = norm_bytes / (norm_ms * 1e-3) / 1e9 if wl.norm_rope else None
     # recorded traffic is for the default workload's launches only
     traffic = _profiled_traffic() if wl.name == WORKLOAD else {}
-    attn_kernel = {64: "attn_fwd_kernel<64,2,8>", 128: "attn_fwd_kernel<128,2,4>", 256: "attn_fwd_kernel<256,1,2>"}[wl.D]
+    attn_kernel = _attn_kernel_name(wl)
     masks = []
     if inp.kv_len is not None:
         masks.append("key padding kv_len=%s" % list(map(int, inp.kv_len)))
@@ -330,6 +330,20 @@ def run_gpu(args):
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+# The library's choice of attention kernel: one query tile per CTA (Q held in
+# tensor memory) from 8192 keys on, for head dims 64 and 128; two query tiles
+# per CTA otherwise.  H3ATTN_ATTN_KERNEL=1/2 forces one or the other.
+ONE_TILE_MIN_KEYS = 8192
+
+
+def _attn_kernel_name(wl):
+    sel = os.environ.get("H3ATTN_ATTN_KERNEL", "")
+    one_tile = wl.D in (64, 128) and (sel == "1" or (sel != "2" and wl.Sk >= ONE_TILE_MIN_KEYS))
+    if one_tile:
+        return {64: "attn_pipe_kernel<64,12,2,true>", 128: "attn_pipe_kernel<128,7,2,true>"}[wl.D]
+    return {64: "attn_fwd_kernel<64,2,8>", 128: "attn_fwd_kernel<128,2,4>", 256: "attn_fwd_kernel<256,1,2>"}[wl.D]
 
 
 def _profiled_traffic():

@@ -40,6 +40,14 @@ def full_case(h3, B, Sq, Sk, Hq, Hkv, D, seed=0, causal=False, kv_len=None, q_le
 
 
 # ---------------------------------------------------------------- small / edge cases
+# Every edge case runs on both attention kernels: "1" = one query tile per CTA
+# (Q in tensor memory), "2" = two query tiles per CTA.  Without the override
+# the library picks by key length.
+@pytest.fixture(params=["1", "2"], ids=["one_tile", "two_tiles"])
+def kernel(request, monkeypatch):
+    monkeypatch.setenv("H3ATTN_ATTN_KERNEL", request.param)
+    return request.param
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("B,Sq,Sk,Hq,Hkv,D", [
     (1, 128, 128, 1, 1, 128),    # one tile
@@ -51,13 +59,13 @@ def full_case(h3, B, Sq, Sk, Hq, Hkv, D, seed=0, causal=False, kv_len=None, q_le
     (1, 190, 333, 2, 2, 64),
     (2, 130, 260, 4, 2, 256),
 ])
-def test_dense_shapes(h3, B, Sq, Sk, Hq, Hkv, D):
+def test_dense_shapes(h3, kernel, B, Sq, Sk, Hq, Hkv, D):
     full_case(h3, B, Sq, Sk, Hq, Hkv, D, seed=B * 1000 + Sq, what=f"dense {B},{Sq},{Sk},{Hq},{Hkv},{D}")
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("D", [64, 128, 256])
-def test_causal_and_padding(h3, D):
+def test_causal_and_padding(h3, kernel, D):
     B, S = 3, 389
     kv_len = np.array([389, 150, 1], np.int32)
     causal_b = np.array([1, 0, 1], np.uint8)
@@ -66,7 +74,7 @@ def test_causal_and_padding(h3, D):
 
 
 @pytest.mark.gpu
-def test_bit_mask_and_q_len_and_degenerate(h3):
+def test_bit_mask_and_q_len_and_degenerate(h3, kernel):
     # random packed boolean [Q, K] mask, combined with key padding
     full_case(h3, 2, 200, 333, 2, 2, 128, seed=5, bits_density=0.3, kv_len=np.array([333, 100], np.int32),
               what="bits+pad")
@@ -78,13 +86,13 @@ def test_bit_mask_and_q_len_and_degenerate(h3):
 
 
 @pytest.mark.gpu
-def test_peaky_scores_exercise_rescaling(h3):
+def test_peaky_scores_exercise_rescaling(h3, kernel):
     """Large-magnitude inputs: maxima grow across key tiles, forcing O rescales."""
     full_case(h3, 1, 256, 1024, 2, 2, 128, seed=8, std=4.0, what="peaky")
 
 
 @pytest.mark.gpu
-def test_gqa_equals_repeated_heads_on_gpu(h3):
+def test_gqa_equals_repeated_heads_on_gpu(h3, kernel):
     B, S, Hq, Hkv, D = 1, 256, 8, 2, 128
     q = gen.normal_bshd(B, S, Hq, D, 9, gen.STREAM_Q)
     k = gen.normal_bshd(B, S, Hkv, D, 9, gen.STREAM_K)

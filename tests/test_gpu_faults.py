@@ -12,7 +12,8 @@ from helpers import check_close, from_dev, to_dev
 
 
 @pytest.mark.gpu
-def test_stalled_producer_times_out_and_context_survives(h3, monkeypatch):
+@pytest.mark.parametrize("kernel", ["1", "2"], ids=["one_tile", "two_tiles"])
+def test_stalled_producer_times_out_and_context_survives(h3, monkeypatch, kernel):
     import torch
     B, S, H, D = 1, 256, 1, 128  # one CTA: one wait limit of runtime
     q = gen.normal_bshd(B, S, H, D, 5, gen.STREAM_Q)
@@ -22,6 +23,7 @@ def test_stalled_producer_times_out_and_context_survives(h3, monkeypatch):
     o = torch.full(dq.shape, 7.0, dtype=torch.bfloat16, device="cuda")
     assert h3.h3attn_check_device_status() == h3.H3ATTN_OK
 
+    monkeypatch.setenv("H3ATTN_ATTN_KERNEL", kernel)
     monkeypatch.setenv("H3ATTN_FAULT_INJECT_STALL_PRODUCER", "1")
     monkeypatch.setenv("H3ATTN_WAIT_LIMIT_MS", "200")
     h3.h3attn_prefill(dq, dk, dv, o, 1.0 / np.sqrt(D))

@@ -174,6 +174,7 @@ h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void
   if (!make_bshd_map(&a.tm_q, q, B, Sq, Hq, D) || !make_bshd_map(&a.tm_k, k, B, Sk, Hkv, D) ||
       !make_bshd_map(&a.tm_v, v, B, Sk, Hkv, D))
     return H3ATTN_ERR_LAUNCH;
+  a.q_ptr = static_cast<const uint16_t*>(q);
   a.o = static_cast<uint16_t*>(o);
   a.kv_len = mask ? mask->kv_len : nullptr;
   a.q_len = mask ? mask->q_len : nullptr;
@@ -190,6 +191,9 @@ h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void
   a.wait_limit_ns = wait_limit_ns();
   const char* inj = getenv("H3ATTN_FAULT_INJECT_STALL_PRODUCER");
   a.debug_skip_producer = (inj && inj[0] == '1') ? 1 : 0;
+  // Kernel choice override (tests run every case on both kernels): "1" or "2".
+  const char* kern = getenv("H3ATTN_ATTN_KERNEL");
+  a.kernel = (kern && (kern[0] == '1' || kern[0] == '2')) ? kern[0] - '0' : 0;
   cudaError_t e = h3::launch_attention(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_LAUNCH;
 }

@@ -446,6 +446,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
   }
 }
 
+#include "attn_pipe.cuh"
+
 template <int D, int NQ, int NSTAGE>
 cudaError_t launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   using C = Cfg<D, NQ, NSTAGE>;
@@ -493,9 +495,15 @@ int read_and_clear_status(int* value) {
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
+  // Two kernels for head_dim 64/128: one query tile per CTA with Q in tensor
+  // memory (faster when there are many key tiles to amortise its longer
+  // per-tile chain), or two query tiles per CTA sharing each K/V tile
+  // (faster on short key ranges).  a.kernel: 0 = by key length, 1 = one
+  // query tile, 2 = two query tiles.
+  const bool one_tile = a.kernel == 1 || (a.kernel == 0 && a.Sk >= kOneTileMinKeys);
   switch (a.D) {
-    case 64: return launch_cfg<64, 2, 8>(a, stream);
-    case 128: return launch_cfg<128, 2, 4>(a, stream);
+    case 64: return one_tile ? launch_pipe<64, 12, 2, true>(a, stream) : launch_cfg<64, 2, 8>(a, stream);
+    case 128: return one_tile ? launch_pipe<128, 7, 2, true>(a, stream) : launch_cfg<128, 2, 4>(a, stream);
     case 256: return launch_cfg<256, 1, 2>(a, stream);
     default: return cudaErrorInvalidValue;
   }

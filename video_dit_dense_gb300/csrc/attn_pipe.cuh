@@ -1,0 +1,404 @@
+// Attention kernel with one 128-row query tile per CTA and three score
+// buffers in tensor memory (included by attn_fwd.cu inside its anonymous
+// namespace; uses its helpers).
+//
+// Tensor memory (512 columns): S_0, S_1, S_2 at [0,128), [128,256),
+// [256,384) and O at [384, 384+D).  P_j (bf16 pairs) is written over the
+// first 64 columns of S_{j mod 3}.  The MMA thread issues
+//     S_0, S_1, then per key tile j:  O += P_j V_j,  S_{j+2} = Q K_{j+2}^T
+// S_{j+2} reuses the buffer of tile j-1, whose O += P V was issued one tile
+// earlier, so the thread never waits on a product it has just issued, and
+// the softmax of tile j+1 has the time of O += P_j V_j and S_{j+2} (two
+// 512-cycle products) to finish.
+//
+//   warps 0-3  softmax warpgroup, thread t = query row t = TMEM lane t
+//   warp 4     TMA producer (Q once unless Q lives in TMEM, then K/V in consumption order)
+//   warp 5     MMA issuer; allocates tensor memory
+//   warps 6-7  idle
+template <int D, int NSTAGE, int NS, bool QT>
+struct PipeCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kBlockM * D * 2;
+  static constexpr int kChunkBytes = kBlockM * 128;
+  static constexpr int kSmemQ = QT ? 0 : kTileBytes;  // Q lives in tensor memory when QT
+  static constexpr int kSmemKV = NSTAGE * kTileBytes;
+  static constexpr int kNumS = NS;
+  // q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[NS], p_ready[NS], pv_done[NS], drain
+  static constexpr int kNumBars = 1 + 2 * NSTAGE + 3 * kNumS + 1;
+  static constexpr int kSmemBytes = 1024 + kSmemQ + kSmemKV + kNumBars * 8 + 16;
+  static constexpr int kThreads = 256;
+  static constexpr int kProducerWarp = 4;
+  static constexpr int kMmaWarp = 5;
+  static constexpr int kColO = kNumS * 128;
+  static constexpr int kColQ = kColO + D;  // Q as bf16 pairs, D/2 columns (when QT)
+  static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kBlockN, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+  static_assert(kColO + D + (QT ? D / 2 : 0) <= static_cast<int>(kTmemCols), "tensor memory budget");
+  static_assert(NS == 2 || NS == 3, "two or three score buffers");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(NSTAGE >= 4, "K_{j+2}, V_j and V_{j+1} resident together");
+};
+
+template <int D, int NSTAGE, int NS, bool QT>
+__global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant__ AttnArgs a) {
+  using C = PipeCfg<D, NSTAGE, NS, QT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base;
+  const uint32_t sKV = base + C::kSmemQ;
+  const uint32_t bars = sKV + C::kSmemKV;
+  const uint32_t bar_q_full = bars;
+  auto bar_kv_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto bar_kv_empty = [&](int s) { return bars + 8u * (1 + NSTAGE + s); };
+  // One barrier of each kind per score buffer: a barrier then completes once
+  // per three tiles, and no party can run three tiles ahead of another.
+  auto bar_s_full = [&](int bf) { return bars + 8u * (1 + 2 * NSTAGE + bf); };
+  auto bar_p_ready = [&](int bf) { return bars + 8u * (1 + 2 * NSTAGE + NS + bf); };
+  auto bar_pv_done = [&](int bf) { return bars + 8u * (1 + 2 * NSTAGE + 2 * NS + bf); };
+  const uint32_t bar_drain = bars + 8u * (1 + 2 * NSTAGE + 3 * NS);
+  uint8_t* gmisc = gbase + C::kSmemQ + C::kSmemKV + C::kNumBars * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gmisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: (b, h, 128-row query tile) -------------------------------
+  const int b = blockIdx.z;
+  const int h = blockIdx.y;
+  const int kvh = h / (a.Hq / a.Hkv);
+  const int qb = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // longest (causal) first
+  const int q0 = qb * kBlockM;
+  int kv_lim = a.Sk;
+  if (a.kv_len) kv_lim = min(kv_lim, max(a.kv_len[b], 0));
+  const bool causal = a.causal || (a.causal_b && a.causal_b[b]);
+  int q_lim = a.Sq;
+  if (a.q_len) q_lim = min(q_lim, max(a.q_len[b], 0));
+  int kv_end = kv_lim;
+  if (causal) kv_end = min(kv_end, q0 + kBlockM);
+  const int n_tiles = (q0 >= q_lim || kv_end <= 0) ? 0 : (kv_end + kBlockN - 1) / kBlockN;
+  // Loads are issued in the order the MMA thread consumes them:
+  //   K_0, K_1, V_0, K_2, V_1, K_3, ..., V_{n-3}, K_{n-1}, V_{n-2}, V_{n-1}
+  // so a stage never holds a tile that waits behind a later one, and every
+  // stage is released in load order.  Load index of K_j and V_j:
+  auto ld_k = [](int j) { return j < 2 ? j : 2 * j - 1; };
+  auto ld_v = [n_tiles](int j) { return min(2 * j + 2, 2 * n_tiles - 1); };
+  auto stage_of = [](int load) { return load % NSTAGE; };
+  auto phase_of = [](int load) { return static_cast<uint32_t>((load / NSTAGE) & 1); };
+  // Iteration j visits key tile (j + rot) mod n_tiles.  The online softmax
+  // does not depend on the order of the key tiles; rotating the start by the
+  // query block spreads the CTAs that run at the same time (neighbouring
+  // query blocks of one head) over different K/V tiles instead of having all
+  // of them read the same tile's lines at once.
+  const int rot = n_tiles > 0 ? static_cast<int>(blockIdx.x) % n_tiles : 0;
+  auto tile_of = [rot, n_tiles](int j) { return j + rot < n_tiles ? j + rot : j + rot - n_tiles; };
+  // Tile j uses score buffer j % NS; its barriers complete for the (j / NS)-th time.
+  auto bpar = [](int j) { return static_cast<uint32_t>((j / NS) & 1); };
+
+  WaitCtl ctl{abort_flag, &g_status_word, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
+
+  if (warp == C::kProducerWarp && lane == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(bar_kv_full(s), 1);
+      mbar_init(bar_kv_empty(s), 1);
+    }
+    mbar_init(bar_q_full, QT ? 128 : 1);  // Q: TMA bytes, or the 128 rows stored to TMEM
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(bar_s_full(i), 1);
+      mbar_init(bar_p_ready(i), 128);
+      mbar_init(bar_pv_done(i), 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    prefetch_tmap(&a.tm_q);
+    prefetch_tmap(&a.tm_k);
+    prefetch_tmap(&a.tm_v);
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::kProducerWarp) {
+    // ======================= TMA producer ==================================
+    if (lane == 0 && n_tiles > 0 && !a.debug_skip_producer) {
+      if constexpr (!QT) {
+        mbar_arrive_expect_tx(bar_q_full, C::kSmemQ);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sQ + c * C::kChunkBytes, &a.tm_q, bar_q_full, c * 64, h, q0, b);
+      }
+      int ld = 0;
+      bool ok = true;
+      auto load = [&](int kind, int j) {
+        const int s = stage_of(ld);
+        if (!(ok = mbar_wait(bar_kv_empty(s), phase_of(ld) ^ 1u, ctl))) return;
+        H3_TRACE(kind == 0 ? kEvProdK : kEvProdV, j);
+        mbar_arrive_expect_tx(bar_kv_full(s), C::kTileBytes);
+        const CUtensorMap* m = kind == 0 ? &a.tm_k : &a.tm_v;
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sKV + s * C::kTileBytes + c * C::kChunkBytes, m, bar_kv_full(s), c * 64, kvh,
+                      tile_of(j) * kBlockN, b);
+        ++ld;
+      };
+      load(0, 0);
+      if (ok && n_tiles > 1) load(0, 1);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        load(1, j);
+        if (ok && j + 2 < n_tiles) load(0, j + 2);
+      }
+      // Drain: every issued copy has landed before the CTA can retire.
+      if constexpr (!QT) mbar_wait_drain(bar_q_full, 0, a.wait_limit_ns);
+      for (int i = ld > NSTAGE ? ld - NSTAGE : 0; i < ld; ++i)
+        mbar_wait_drain(bar_kv_full(stage_of(i)), phase_of(i), a.wait_limit_ns);
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ======================= MMA issuer ====================================
+    if (lane == 0 && n_tiles > 0) {
+      bool ok = mbar_wait(bar_q_full, 0, ctl);
+      tc_fence_after();
+      // S_{j mod NS} = Q K_j^T; the buffer last held P of tile j-NS, so that
+      // tile's O += P V must have completed.
+      auto issue_qk = [&](int j) -> bool {
+        const int ld = ld_k(j);
+        const int s = stage_of(ld);
+        if (!mbar_wait(bar_kv_full(s), phase_of(ld), ctl)) return false;
+        H3_TRACE(kEvMmaK, j);
+        if (j >= NS && !mbar_wait(bar_pv_done(j % NS), bpar(j - NS), ctl)) return false;
+        tc_fence_after();
+        H3_TRACE(kEvMmaQK0, j);
+        const uint32_t kb = sKV + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          if constexpr (QT) {
+            // A = Q from tensor memory: channels [16kk, 16kk+16) are columns [8kk, 8kk+8)
+            mma_ts(tmem + (j % NS) * 128, tmem + C::kColQ + kk * 8, sdesc_sw128(kb + off, 16, 1024),
+                   C::kIdescQK, kk > 0 ? 1u : 0u);
+          } else {
+            mma_ss(tmem + (j % NS) * 128, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                   C::kIdescQK, kk > 0 ? 1u : 0u);
+          }
+        }
+        tc_commit(bar_s_full(j % NS));
+        tc_commit(bar_kv_empty(s));
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      if (ok && n_tiles > 1) ok = issue_qk(1);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int bf = j % NS;
+        const int ld = ld_v(j);
+        const int s = stage_of(ld);
+        if (!(ok = mbar_wait(bar_kv_full(s), phase_of(ld), ctl))) break;
+        H3_TRACE(kEvMmaV, j);
+        if (!(ok = mbar_wait(bar_p_ready(bf), bpar(j), ctl))) break;
+        H3_TRACE(kEvMmaPV0, j);
+        tc_fence_after();
+        const uint32_t vb = sKV + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          mma_ts(tmem + C::kColO, tmem + bf * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024),
+                 C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar_pv_done(bf));
+        tc_commit(bar_kv_empty(s));
+        if (j + 2 < n_tiles) ok = issue_qk(j + 2);
+      }
+      // Drain every MMA issued by this thread before tensor memory is freed.
+      tc_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0, a.wait_limit_ns);
+    }
+  } else if (warp < 4) {
+    // ======================= softmax / correction / epilogue ===============
+    const int wq = warp & 3;         // lane quarter of tensor memory
+    const int t = wq * 32 + lane;    // row within the tile
+    const int row = q0 + t;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tO = tmem + lane_off + C::kColO;
+    const float sl = a.scale_log2;
+    const int64_t bit_words = (a.Sk + 31) / 32;
+    float m_ref = -INFINITY;  // running max in scaled (log2) units
+    float l = 0.0f;
+    bool ok = true;
+    if constexpr (QT) {
+      // This thread's query row (D bf16) into tensor-memory lane t as bf16
+      // pairs, the A-operand layout of S = Q K^T; rows past Sq are zeros.
+      if (n_tiles > 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q_ptr + ((static_cast<int64_t>(b) * a.Sq + row) * a.Hq + h) * D);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t w[32];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 x = row < a.Sq ? __ldg(src + c * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
+            w[4 * v] = x.x;
+            w[4 * v + 1] = x.y;
+            w[4 * v + 2] = x.z;
+            w[4 * v + 3] = x.w;
+          }
+          tmem_st32(tmem + lane_off + C::kColQ + c * 32, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_q_full);
+      }
+    }
+    for (int j = 0; j < n_tiles; ++j) {
+      const int bf = j % NS;
+      ok = mbar_wait(bar_s_full(bf), bpar(j), ctl);
+      if (t == 0) H3_TRACE(kEvSmS0, j);
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_off + bf * 128;
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+      if (t == 0) H3_TRACE(kEvSmLd0, j);
+      float s[kBlockN];
+#pragma unroll
+      for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      const int kbase = tile_of(j) * kBlockN;
+      const bool need_mask = (kbase + kBlockN > kv_lim) || (causal && kbase + kBlockN - 1 > q0) || a.bits;
+      if (need_mask) {
+        int lim = kv_lim - kbase;
+        if (causal) lim = min(lim, row + 1 - kbase);
+        uint32_t wbits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+        if (a.bits && row < a.Sq) {
+          const uint32_t* br = a.bits + (static_cast<int64_t>(b) * a.Sq + row) * bit_words;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int64_t wi = kbase / 32 + w;
+            wbits[w] = wi < bit_words ? br[wi] : 0u;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c) {
+          const bool allowed = (c < lim) && ((wbits[c >> 5] >> (c & 31)) & 1u);
+          s[c] = allowed ? s[c] : -INFINITY;
+        }
+      }
+      // row max: 3-input max in 8 independent chains
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+      for (int c = 16; c < kBlockN; c += 16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+      }
+      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+      const float mt_s = mt * sl;
+      const bool grow = mt_s > m_ref + kRescaleThreshold;
+      float alpha = 1.0f;
+      if (grow) {
+        alpha = ex2(m_ref - mt_s);  // m_ref = -inf gives 0
+        l *= alpha;
+        m_ref = mt_s;
+      }
+      if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
+        // O must hold every P V product of tiles < j before it is rescaled.
+        ok = mbar_wait(bar_pv_done((j - 1) % NS), bpar(j - 1), ctl);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+        tmem_st_wait();
+      }
+      const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
+      // p = exp2(s * scale*log2e - m): packed FMA, ex2, packed row-sum
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t p[2][32];
+#pragma unroll
+      for (int c = 0; c < kBlockN; c += 2) {
+        float t0, t1;
+        ffma2(t0, t1, s[c], s[c + 1], sl, sl, -mu, -mu);
+        const float p0 = ex2(t0);
+        const float p1 = ex2(t1);
+        const int a2 = ((c >> 1) & 3) * 2;
+        fadd2(ls[a2], ls[a2 + 1], ls[a2], ls[a2 + 1], p0, p1);
+        p[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
+      }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      if (t == 0) H3_TRACE(kEvSmExp0, j);
+      tmem_st32(tS, p[0]);
+      tmem_st32(tS + 32, p[1]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_p_ready(bf));
+      if (t == 0) H3_TRACE(kEvSmArr0, j);
+    }
+    // ---- epilogue: O / l -> bf16 ------------------------------------------
+    if (ok && n_tiles > 0) {
+      ok = mbar_wait(bar_pv_done((n_tiles - 1) % NS), bpar(n_tiles - 1), ctl);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      tc_fence_after();
+    }
+    if (ok) {
+      const bool live_row = row < a.Sq;
+      const bool zero_row = row >= q_lim || n_tiles == 0 || !(l > 0.0f);
+      const float inv = zero_row ? 0.0f : 1.0f / l;
+      uint16_t* orow = a.o + ((static_cast<int64_t>(b) * a.Sq + row) * a.Hq + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+        }
+        if (live_row) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = zero_row ? 0.0f : __uint_as_float(o[v * 8 + e]) * inv;
+            dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                pack_bf16x2(f[6], f[7]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, int NSTAGE, int NS, bool QT>
+cudaError_t launch_pipe(const AttnArgs& a, cudaStream_t stream) {
+  using C = PipeCfg<D, NSTAGE, NS, QT>;
+  auto kern = attn_pipe_kernel<D, NSTAGE, NS, QT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Sq + kBlockM - 1) / kBlockM, a.Hq, a.B);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}

@@ -54,6 +54,7 @@ cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
 // ---- dense prefill attention ----
 struct AttnArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D (D, H, S, B) bf16 maps, 64-element inner box, 128B swizzle
+  const uint16_t* q_ptr;         // q itself (kernels that stage Q through registers)
   uint16_t* o;
   const int32_t* kv_len;
   const int32_t* q_len;
@@ -64,7 +65,10 @@ struct AttnArgs {
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int debug_skip_producer;  // fault injection for the bounded-wait test: 1 = never load K/V
+  int kernel;               // 0 = choose by key length, 1 = one query tile per CTA, 2 = two
 };
+// Key length from which the one-query-tile kernel is chosen (head_dim 64/128).
+constexpr int kOneTileMinKeys = 8192;
 // Box rows of the Q/K/V maps built by the launcher.
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;

@@ -54,6 +54,44 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// try_wait with an explicit suspend-time hint (nanoseconds).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+#ifndef H3ATTN_WAIT_MODE
+#define H3ATTN_WAIT_MODE 0  // 0: try_wait, 1: test_wait spin, 2: try_wait with a short suspend hint
+#endif
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+#if H3ATTN_WAIT_MODE == 1
+  return mbar_test_wait(bar, parity);
+#elif H3ATTN_WAIT_MODE == 2
+  return mbar_try_wait_hint(bar, parity, 20);
+#else
+  return mbar_try_wait(bar, parity);
+#endif
+}
+
 // Shared abort/timeout bookkeeping of one CTA.
 struct WaitCtl {
   volatile uint32_t* abort_flag;  // shared memory: nonzero once any waiter gave up
@@ -67,7 +105,7 @@ __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, co
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_poll(bar, parity)) return true;
     if (*ctl.abort_flag) return false;
     if (globaltimer_ns() - t0 > ctl.limit_ns) {
       *ctl.abort_flag = 1u;
@@ -80,7 +118,7 @@ __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, co
 // Wait until the phase with parity `parity` of `bar` has completed.
 // Returns false if the CTA is aborting (this waiter or another timed out).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_poll(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, ctl);
 }
 
