@@ -77,26 +77,42 @@ def _workload_numbers(wl):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling while the timed region runs."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock/throttle sampling; only samples stamped inside the
+    timed region (host wall-clock window set by window()) are summarised."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         fd, self.path = tempfile.mkstemp(prefix="h3clk", suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         time.sleep(0.3)
+
+    def window(self, t0: float, t1: float):
+        self.t0, self.t1 = t0, t1
+
+    @staticmethod
+    def _epoch(stamp: str):
+        from datetime import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
 
     def stop(self):
         if self.proc is None:
@@ -110,16 +126,32 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
+                if len(parts) >= 10:
                     rows.append(parts)
         os.unlink(self.path)
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        return self.summarise(rows)
+
+    def summarise(self, rows):
+        """rows: split CSV lines of QUERY; returns the clocks record."""
+        inside = [r for r in rows if self.t0 is not None and (t := self._epoch(r[0])) is not None
+                  and self.t0 <= t <= self.t1]
+        use = inside if inside else rows
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for r in use if (v := num(r[2])) is not None]
+        smax = [v for r in use if (v := num(r[3])) is not None]
+        power = [v for r in use if (v := num(r[4])) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[6 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "whole sampler run (no sample inside the timed region)",
+                "power_w_median": statistics.median(power) if power else None,
+                "power_w_max": max(power) if power else None}
 
 
 def run_gpu(args):
@@ -180,6 +212,7 @@ def run_gpu(args):
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
+    wall0 = time.time()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -193,6 +226,7 @@ def run_gpu(args):
         ev[i][2].record(stream)
     t_end.record(stream)
     barrier()
+    clocks.window(wall0, time.time())
     clk = clocks.stop()
     st = h3.h3attn_check_device_status(stream)
     if st != 0:
@@ -442,7 +476,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)

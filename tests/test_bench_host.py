@@ -18,3 +18,21 @@ def test_nominal_flops_of_headline_shape():
     flops, norm_bytes = bench._workload_numbers(gen.WORKLOADS["long_video_h24"])
     assert flops == 4.0 * 32760 * 32760 * 24 * 128
     assert norm_bytes == 2.0 * (32760 * 48) * 128 * 2 + 2.0 * 32760 * 48 * 4 + 2.0 * 128 * 4
+
+
+def test_clock_summary_keeps_only_the_timed_window():
+    c = bench.ClockSampler(0)
+    t0 = c._epoch("2026/12/02 10:00:01.000")
+    c.window(t0, t0 + 1.0)
+
+    def row(stamp, mhz, capped):
+        return [stamp, "0", str(mhz), "2070", "900.5", "0x0", "Not Active", "Not Active", "Not Active",
+                "Active" if capped else "Not Active"]
+    rows = [row("2026/12/02 10:00:00.500", 2070, False),      # before the window: idle
+            row("2026/12/02 10:00:01.100", 1800, True),
+            row("2026/12/02 10:00:01.600", 1700, True),
+            row("2026/12/02 10:00:01.900", 1750, False),
+            row("2026/12/02 10:00:02.500", 2070, False)]      # after the window
+    rec = c.summarise(rows)
+    assert rec["samples"] == 3 and rec["sm_mhz"] == 1750 and rec["sm_max_mhz"] == 2070
+    assert rec["reasons"] == ["sw_power_cap"] and rec["window"] == "timed region"
