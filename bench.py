@@ -376,7 +376,7 @@ def _attn_kernel_name(wl):
     sel = os.environ.get("H3ATTN_ATTN_KERNEL", "")
     one_tile = wl.D in (64, 128) and (sel == "1" or (sel != "2" and wl.Sk >= ONE_TILE_MIN_KEYS))
     if one_tile:
-        return {64: "attn_pipe_kernel<64,12,2,true>", 128: "attn_pipe_kernel<128,7,2,true>"}[wl.D]
+        return {64: "attn_pipe_kernel<64,12>", 128: "attn_pipe_kernel<128,7>"}[wl.D]
     return {64: "attn_fwd_kernel<64,2,8>", 128: "attn_fwd_kernel<128,2,4>", 256: "attn_fwd_kernel<256,1,2>"}[wl.D]
 
 

@@ -502,8 +502,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   // query tile, 2 = two query tiles.
   const bool one_tile = a.kernel == 1 || (a.kernel == 0 && a.Sk >= kOneTileMinKeys);
   switch (a.D) {
-    case 64: return one_tile ? launch_pipe<64, 12, 2, true>(a, stream) : launch_cfg<64, 2, 8>(a, stream);
-    case 128: return one_tile ? launch_pipe<128, 7, 2, true>(a, stream) : launch_cfg<128, 2, 4>(a, stream);
+    case 64: return one_tile ? launch_pipe<64, 12>(a, stream) : launch_cfg<64, 2, 8>(a, stream);
+    case 128: return one_tile ? launch_pipe<128, 7>(a, stream) : launch_cfg<128, 2, 4>(a, stream);
     case 256: return launch_cfg<256, 1, 2>(a, stream);
     default: return cudaErrorInvalidValue;
   }

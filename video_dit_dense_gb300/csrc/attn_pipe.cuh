@@ -1,64 +1,77 @@
-// Attention kernel with one 128-row query tile per CTA and three score
-// buffers in tensor memory (included by attn_fwd.cu inside its anonymous
-// namespace; uses its helpers).
+// Attention kernel with one 128-row query tile per CTA, two MMA-issuing
+// threads and a separate P buffer (included by attn_fwd.cu inside its
+// anonymous namespace; uses its helpers).
 //
-// Tensor memory (512 columns): S_0, S_1, S_2 at [0,128), [128,256),
-// [256,384) and O at [384, 384+D).  P_j (bf16 pairs) is written over the
-// first 64 columns of S_{j mod 3}.  The MMA thread issues
-//     S_0, S_1, then per key tile j:  O += P_j V_j,  S_{j+2} = Q K_{j+2}^T
-// S_{j+2} reuses the buffer of tile j-1, whose O += P V was issued one tile
-// earlier, so the thread never waits on a product it has just issued, and
-// the softmax of tile j+1 has the time of O += P_j V_j and S_{j+2} (two
-// 512-cycle products) to finish.
+// Tensor memory (512 columns x 128 lanes):
+//   S_0, S_1  [0,128), [128,256)     scores of even / odd key tiles (fp32)
+//   P         [256, 320)             probabilities of the current tile (bf16 pairs)
+//   O         [320, 320+D)           output accumulator (fp32)
+//   Q         [320+D, 320+D+D/2)     this CTA's query rows (bf16 pairs), the A
+//                                    operand of S = Q K^T
+//
+// Score tile S_j lives in buffer S_{j mod 2}.  Once P_j is ready, MMA thread
+// p = j mod 2 issues the burst
+//     O += P_j V_j;   S_{j+3} = Q K_{j+3}^T  into S_{(j+1) mod 2}
+// (the second half waits until softmax j+1 has read S_{j+1} out of that
+// buffer, which it does at the start of its turn).  The tensor pipe thus runs
+// the product that frees P right away and computes scores three tiles ahead,
+// so the softmax warpgroup, which handles the tiles in order, finds S_{j+1}
+// ready when it finishes tile j and finds the P buffer free when it wants to
+// write P_{j+1}.  Prologue: S_0 (thread 0), S_1 and S_2 (thread 1).
+// Two issuing threads on two SM sub-partitions alternate these bursts: while
+// one does its commits and barrier polls (slow when it shares a sub-partition
+// with a busy softmax warp) the other keeps the tensor pipe fed.
+//
+// P has a single buffer, so softmax j writes P_j only after O += P_{j-1} V_{j-1}
+// has completed; this also makes the O += P V products strictly sequential.
 //
 //   warps 0-3  softmax warpgroup, thread t = query row t = TMEM lane t
-//   warp 4     TMA producer (Q once unless Q lives in TMEM, then K/V in consumption order)
-//   warp 5     MMA issuer; allocates tensor memory
-//   warps 6-7  idle
-template <int D, int NSTAGE, int NS, bool QT>
+//   warp 4     TMA producer: K_0, K_1, K_2, then K_{j+3}, V_j for j = 0, 1, ...
+//   warps 5-6  MMA issuers for even / odd key tiles (warp 5 allocates TMEM)
+//   warp 7     idle
+template <int D, int NSTAGE>
 struct PipeCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kBlockM * D * 2;
   static constexpr int kChunkBytes = kBlockM * 128;
-  static constexpr int kSmemQ = QT ? 0 : kTileBytes;  // Q lives in tensor memory when QT
   static constexpr int kSmemKV = NSTAGE * kTileBytes;
-  static constexpr int kNumS = NS;
-  // q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[NS], p_ready[NS], pv_done[NS], drain
-  static constexpr int kNumBars = 1 + 2 * NSTAGE + 3 * kNumS + 1;
-  static constexpr int kSmemBytes = 1024 + kSmemQ + kSmemKV + kNumBars * 8 + 16;
+  // q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_read[2], p_ready[2], pv_done[2], drain[2]
+  static constexpr int kNumBars = 1 + 2 * NSTAGE + 10;
+  static constexpr int kSmemBytes = 1024 + kSmemKV + kNumBars * 8 + 16;
   static constexpr int kThreads = 256;
   static constexpr int kProducerWarp = 4;
-  static constexpr int kMmaWarp = 5;
-  static constexpr int kColO = kNumS * 128;
-  static constexpr int kColQ = kColO + D;  // Q as bf16 pairs, D/2 columns (when QT)
+  static constexpr int kMmaWarp = 5;  // and kMmaWarp + 1
+  static constexpr int kColP = 256;
+  static constexpr int kColO = 320;
+  static constexpr int kColQ = kColO + D;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kBlockN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
-  static_assert(kColO + D + (QT ? D / 2 : 0) <= static_cast<int>(kTmemCols), "tensor memory budget");
-  static_assert(NS == 2 || NS == 3, "two or three score buffers");
+  static_assert(kColQ + D / 2 <= static_cast<int>(kTmemCols), "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(NSTAGE >= 4, "K_{j+2}, V_j and V_{j+1} resident together");
+  static_assert(NSTAGE >= 4, "K_{j+3}, V_j and the other thread's pair resident together");
 };
 
-template <int D, int NSTAGE, int NS, bool QT>
+template <int D, int NSTAGE>
 __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant__ AttnArgs a) {
-  using C = PipeCfg<D, NSTAGE, NS, QT>;
+  using C = PipeCfg<D, NSTAGE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base;
-  const uint32_t sKV = base + C::kSmemQ;
+  const uint32_t sKV = base;
   const uint32_t bars = sKV + C::kSmemKV;
   const uint32_t bar_q_full = bars;
   auto bar_kv_full = [&](int s) { return bars + 8u * (1 + s); };
   auto bar_kv_empty = [&](int s) { return bars + 8u * (1 + NSTAGE + s); };
-  // One barrier of each kind per score buffer: a barrier then completes once
-  // per three tiles, and no party can run three tiles ahead of another.
-  auto bar_s_full = [&](int bf) { return bars + 8u * (1 + 2 * NSTAGE + bf); };
-  auto bar_p_ready = [&](int bf) { return bars + 8u * (1 + 2 * NSTAGE + NS + bf); };
-  auto bar_pv_done = [&](int bf) { return bars + 8u * (1 + 2 * NSTAGE + 2 * NS + bf); };
-  const uint32_t bar_drain = bars + 8u * (1 + 2 * NSTAGE + 3 * NS);
-  uint8_t* gmisc = gbase + C::kSmemQ + C::kSmemKV + C::kNumBars * 8;
+  // Per parity p = j mod 2 of key tile j: s_full (S_j computed into S_p),
+  // s_read (softmax has read S_j out of S_p), p_ready (P_j written), pv_done
+  // (O += P_j V_j complete); drain: end of MMA thread p.
+  auto bar_s_full = [&](int p) { return bars + 8u * (1 + 2 * NSTAGE + p); };
+  auto bar_s_read = [&](int p) { return bars + 8u * (3 + 2 * NSTAGE + p); };
+  auto bar_p_ready = [&](int p) { return bars + 8u * (5 + 2 * NSTAGE + p); };
+  auto bar_pv_done = [&](int p) { return bars + 8u * (7 + 2 * NSTAGE + p); };
+  auto bar_drain = [&](int p) { return bars + 8u * (9 + 2 * NSTAGE + p); };
+  uint8_t* gmisc = gbase + C::kSmemKV + C::kNumBars * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gmisc + 4);
 
@@ -79,12 +92,12 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   int kv_end = kv_lim;
   if (causal) kv_end = min(kv_end, q0 + kBlockM);
   const int n_tiles = (q0 >= q_lim || kv_end <= 0) ? 0 : (kv_end + kBlockN - 1) / kBlockN;
-  // Loads are issued in the order the MMA thread consumes them:
-  //   K_0, K_1, V_0, K_2, V_1, K_3, ..., V_{n-3}, K_{n-1}, V_{n-2}, V_{n-1}
-  // so a stage never holds a tile that waits behind a later one, and every
-  // stage is released in load order.  Load index of K_j and V_j:
-  auto ld_k = [](int j) { return j < 2 ? j : 2 * j - 1; };
-  auto ld_v = [n_tiles](int j) { return min(2 * j + 2, 2 * n_tiles - 1); };
+  // Load order = consumption order: K_0, K_1, K_2, then K_{j+3} (if any) and
+  // V_j for j = 0, 1, ...  Load index of V_j: the K loads up to
+  // K_{min(j+3, n-1)} and the V loads before it; K_j (j >= 3) sits right
+  // before V_{j-3}.
+  auto ld_v = [n_tiles](int j) { return min(j + 4, n_tiles) + j; };
+  auto ld_k = [](int j) { return j < 3 ? j : 2 * j - 3; };
   auto stage_of = [](int load) { return load % NSTAGE; };
   auto phase_of = [](int load) { return static_cast<uint32_t>((load / NSTAGE) & 1); };
   // Iteration j visits key tile (j + rot) mod n_tiles.  The online softmax
@@ -94,8 +107,8 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   // of them read the same tile's lines at once.
   const int rot = n_tiles > 0 ? static_cast<int>(blockIdx.x) % n_tiles : 0;
   auto tile_of = [rot, n_tiles](int j) { return j + rot < n_tiles ? j + rot : j + rot - n_tiles; };
-  // Tile j uses score buffer j % NS; its barriers complete for the (j / NS)-th time.
-  auto bpar = [](int j) { return static_cast<uint32_t>((j / NS) & 1); };
+  // Tile j's barriers of parity j % 2 complete for the (j / 2)-th time.
+  auto bpar = [](int j) { return static_cast<uint32_t>((j >> 1) & 1); };
 
   WaitCtl ctl{abort_flag, &g_status_word, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
 
@@ -104,16 +117,16 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
-    mbar_init(bar_q_full, QT ? 128 : 1);  // Q: TMA bytes, or the 128 rows stored to TMEM
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(bar_s_full(i), 1);
-      mbar_init(bar_p_ready(i), 128);
-      mbar_init(bar_pv_done(i), 1);
+    mbar_init(bar_q_full, 128);  // the 128 query rows stored to tensor memory
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(bar_s_full(p), 1);
+      mbar_init(bar_s_read(p), 128);
+      mbar_init(bar_p_ready(p), 128);
+      mbar_init(bar_pv_done(p), 1);
+      mbar_init(bar_drain(p), 1);
     }
-    mbar_init(bar_drain, 1);
     *abort_flag = 0u;
     fence_barrier_init();
-    prefetch_tmap(&a.tm_q);
     prefetch_tmap(&a.tm_k);
     prefetch_tmap(&a.tm_v);
   }
@@ -129,11 +142,6 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   if (warp == C::kProducerWarp) {
     // ======================= TMA producer ==================================
     if (lane == 0 && n_tiles > 0 && !a.debug_skip_producer) {
-      if constexpr (!QT) {
-        mbar_arrive_expect_tx(bar_q_full, C::kSmemQ);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(sQ + c * C::kChunkBytes, &a.tm_q, bar_q_full, c * 64, h, q0, b);
-      }
       int ld = 0;
       bool ok = true;
       auto load = [&](int kind, int j) {
@@ -147,73 +155,65 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
                       tile_of(j) * kBlockN, b);
         ++ld;
       };
-      load(0, 0);
-      if (ok && n_tiles > 1) load(0, 1);
+      for (int j = 0; ok && j < 3 && j < n_tiles; ++j) load(0, j);
       for (int j = 0; ok && j < n_tiles; ++j) {
-        load(1, j);
-        if (ok && j + 2 < n_tiles) load(0, j + 2);
+        if (j + 3 < n_tiles) load(0, j + 3);
+        if (ok) load(1, j);
       }
       // Drain: every issued copy has landed before the CTA can retire.
-      if constexpr (!QT) mbar_wait_drain(bar_q_full, 0, a.wait_limit_ns);
       for (int i = ld > NSTAGE ? ld - NSTAGE : 0; i < ld; ++i)
         mbar_wait_drain(bar_kv_full(stage_of(i)), phase_of(i), a.wait_limit_ns);
     }
-  } else if (warp == C::kMmaWarp) {
-    // ======================= MMA issuer ====================================
-    if (lane == 0 && n_tiles > 0) {
+  } else if (warp == C::kMmaWarp || warp == C::kMmaWarp + 1) {
+    // ======================= MMA issuers, one per tile parity ==============
+    const int p = warp - C::kMmaWarp;
+    if (lane == 0 && n_tiles > p) {
       bool ok = mbar_wait(bar_q_full, 0, ctl);
       tc_fence_after();
-      // S_{j mod NS} = Q K_j^T; the buffer last held P of tile j-NS, so that
-      // tile's O += P V must have completed.
-      auto issue_qk = [&](int j) -> bool {
-        const int ld = ld_k(j);
-        const int s = stage_of(ld);
+      // S_{i mod 2} = Q K_i^T (A = Q from tensor memory: channels
+      // [16kk, 16kk+16) are columns [8kk, 8kk+8) of the Q region).
+      auto issue_qk = [&](int i) -> bool {
+        const int ld = ld_k(i), s = stage_of(ld);
         if (!mbar_wait(bar_kv_full(s), phase_of(ld), ctl)) return false;
-        H3_TRACE(kEvMmaK, j);
-        if (j >= NS && !mbar_wait(bar_pv_done(j % NS), bpar(j - NS), ctl)) return false;
+        // S_{i-2} has been read out of the buffer
+        if (i >= 2 && !mbar_wait(bar_s_read(i & 1), bpar(i - 2), ctl)) return false;
         tc_fence_after();
-        H3_TRACE(kEvMmaQK0, j);
+        H3_TRACE(kEvMmaQK0, i);
         const uint32_t kb = sKV + s * C::kTileBytes;
+        const uint32_t tS = tmem + (i & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          if constexpr (QT) {
-            // A = Q from tensor memory: channels [16kk, 16kk+16) are columns [8kk, 8kk+8)
-            mma_ts(tmem + (j % NS) * 128, tmem + C::kColQ + kk * 8, sdesc_sw128(kb + off, 16, 1024),
-                   C::kIdescQK, kk > 0 ? 1u : 0u);
-          } else {
-            mma_ss(tmem + (j % NS) * 128, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                   C::kIdescQK, kk > 0 ? 1u : 0u);
-          }
+          mma_ts(tS, tmem + C::kColQ + kk * 8, sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar_s_full(j % NS));
+        tc_commit(bar_s_full(i & 1));
         tc_commit(bar_kv_empty(s));
         return true;
       };
-      if (ok) ok = issue_qk(0);
-      if (ok && n_tiles > 1) ok = issue_qk(1);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int bf = j % NS;
-        const int ld = ld_v(j);
-        const int s = stage_of(ld);
-        if (!(ok = mbar_wait(bar_kv_full(s), phase_of(ld), ctl))) break;
+      // prologue: S_0 on thread 0; S_1 and S_2 on thread 1
+      if (ok) ok = issue_qk(p);
+      if (ok && p == 1 && n_tiles > 2) ok = issue_qk(2);
+      for (int j = p; ok && j < n_tiles; j += 2) {
+        const int ldv = ld_v(j), sv = stage_of(ldv);
+        if (!(ok = mbar_wait(bar_kv_full(sv), phase_of(ldv), ctl))) break;
         H3_TRACE(kEvMmaV, j);
-        if (!(ok = mbar_wait(bar_p_ready(bf), bpar(j), ctl))) break;
+        if (!(ok = mbar_wait(bar_p_ready(p), bpar(j), ctl))) break;
         H3_TRACE(kEvMmaPV0, j);
         tc_fence_after();
-        const uint32_t vb = sKV + s * C::kTileBytes;
+        const uint32_t vb = sKV + sv * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          mma_ts(tmem + C::kColO, tmem + bf * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024),
+          mma_ts(tmem + C::kColO, tmem + C::kColP + kk * 8, sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024),
                  C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(bar_pv_done(bf));
-        tc_commit(bar_kv_empty(s));
-        if (j + 2 < n_tiles) ok = issue_qk(j + 2);
+        tc_commit(bar_pv_done(p));
+        tc_commit(bar_kv_empty(sv));
+        H3_TRACE(kEvMmaPV1, j);
+        if (j + 3 < n_tiles) ok = issue_qk(j + 3);
       }
       // Drain every MMA issued by this thread before tensor memory is freed.
-      tc_commit(bar_drain);
-      mbar_wait_drain(bar_drain, 0, a.wait_limit_ns);
+      tc_commit(bar_drain(p));
+      mbar_wait_drain(bar_drain(p), 0, a.wait_limit_ns);
     }
   } else if (warp < 4) {
     // ======================= softmax / correction / epilogue ===============
@@ -222,50 +222,51 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
     const int row = q0 + t;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tO = tmem + lane_off + C::kColO;
+    const uint32_t tP = tmem + lane_off + C::kColP;
     const float sl = a.scale_log2;
     const int64_t bit_words = (a.Sk + 31) / 32;
     float m_ref = -INFINITY;  // running max in scaled (log2) units
     float l = 0.0f;
     bool ok = true;
-    if constexpr (QT) {
-      // This thread's query row (D bf16) into tensor-memory lane t as bf16
-      // pairs, the A-operand layout of S = Q K^T; rows past Sq are zeros.
-      if (n_tiles > 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q_ptr + ((static_cast<int64_t>(b) * a.Sq + row) * a.Hq + h) * D);
+    // O += P V of tile i has completed
+    auto wait_pv = [&](int i) { return mbar_wait(bar_pv_done(i & 1), bpar(i), ctl); };
+    // This thread's query row (D bf16) into tensor-memory lane t as bf16
+    // pairs, the A-operand layout of S = Q K^T; rows past Sq are zeros.
+    if (n_tiles > 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.q_ptr + ((static_cast<int64_t>(b) * a.Sq + row) * a.Hq + h) * D);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t w[32];
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t w[32];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint4 x = row < a.Sq ? __ldg(src + c * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
-            w[4 * v] = x.x;
-            w[4 * v + 1] = x.y;
-            w[4 * v + 2] = x.z;
-            w[4 * v + 3] = x.w;
-          }
-          tmem_st32(tmem + lane_off + C::kColQ + c * 32, w);
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = row < a.Sq ? __ldg(src + c * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * v] = x.x;
+          w[4 * v + 1] = x.y;
+          w[4 * v + 2] = x.z;
+          w[4 * v + 3] = x.w;
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar_q_full);
+        tmem_st32(tmem + lane_off + C::kColQ + c * 32, w);
       }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_q_full);
     }
     for (int j = 0; j < n_tiles; ++j) {
-      const int bf = j % NS;
-      ok = mbar_wait(bar_s_full(bf), bpar(j), ctl);
+      ok = mbar_wait(bar_s_full(j & 1), bpar(j), ctl);
       if (t == 0) H3_TRACE(kEvSmS0, j);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t tS = tmem + lane_off + bf * 128;
+      const uint32_t tS = tmem + lane_off + (j & 1) * 128;
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+      tc_fence_before();
+      mbar_arrive(bar_s_read(j & 1));  // S_{j mod 2} may be overwritten by S_{j+2}
       if (t == 0) H3_TRACE(kEvSmLd0, j);
       float s[kBlockN];
 #pragma unroll
@@ -310,8 +311,9 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
         m_ref = mt_s;
       }
       if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
-        // O must hold every P V product of tiles < j before it is rescaled.
-        ok = mbar_wait(bar_pv_done((j - 1) % NS), bpar(j - 1), ctl);
+        // O must hold every P V product of tiles < j before it is rescaled;
+        // the products are sequential, so the last one completing is enough.
+        ok = wait_pv(j - 1);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
           ok = false;
           break;
@@ -331,7 +333,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
       // p = exp2(s * scale*log2e - m): packed FMA, ex2, packed row-sum
       float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t p[2][32];
+      uint32_t pr[2][32];
 #pragma unroll
       for (int c = 0; c < kBlockN; c += 2) {
         float t0, t1;
@@ -340,21 +342,29 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
         const float p1 = ex2(t1);
         const int a2 = ((c >> 1) & 3) * 2;
         fadd2(ls[a2], ls[a2 + 1], ls[a2], ls[a2 + 1], p0, p1);
-        p[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
+        pr[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
       }
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       if (t == 0) H3_TRACE(kEvSmExp0, j);
-      tmem_st32(tS, p[0]);
-      tmem_st32(tS + 32, p[1]);
+      // The single P buffer is free once O += P_{j-1} V_{j-1} has completed.
+      if (j > 0) {
+        ok = wait_pv(j - 1);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st32(tP, pr[0]);
+      tmem_st32(tP + 32, pr[1]);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_p_ready(bf));
+      mbar_arrive(bar_p_ready(j & 1));
       if (t == 0) H3_TRACE(kEvSmArr0, j);
     }
     // ---- epilogue: O / l -> bf16 ------------------------------------------
     if (ok && n_tiles > 0) {
-      ok = mbar_wait(bar_pv_done((n_tiles - 1) % NS), bpar(n_tiles - 1), ctl);
-      ok = __all_sync(0xFFFFFFFFu, ok);
+      ok = __all_sync(0xFFFFFFFFu, wait_pv(n_tiles - 1));
       tc_fence_after();
     }
     if (ok) {
@@ -392,10 +402,10 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   }
 }
 
-template <int D, int NSTAGE, int NS, bool QT>
+template <int D, int NSTAGE>
 cudaError_t launch_pipe(const AttnArgs& a, cudaStream_t stream) {
-  using C = PipeCfg<D, NSTAGE, NS, QT>;
-  auto kern = attn_pipe_kernel<D, NSTAGE, NS, QT>;
+  using C = PipeCfg<D, NSTAGE>;
+  auto kern = attn_pipe_kernel<D, NSTAGE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Sq + kBlockM - 1) / kBlockM, a.Hq, a.B);
