@@ -44,6 +44,9 @@ namespace {
 
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+// A tile row sum at most 2^kRescaleThreshold bounds every probability of the
+// tile by 2^kRescaleThreshold: no score exceeds the running max by more.
+constexpr float kFastPassSumLimit = 256.0f;
 
 template <int D, int NQ, int NSTAGE>
 struct Cfg {

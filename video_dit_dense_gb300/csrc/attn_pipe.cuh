@@ -260,92 +260,111 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       }
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + (j & 1) * 128;
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-      tc_fence_before();
-      mbar_arrive(bar_s_read(j & 1));  // S_{j mod 2} may be overwritten by S_{j+2}
-      if (t == 0) H3_TRACE(kEvSmLd0, j);
-      float s[kBlockN];
-#pragma unroll
-      for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
-
       const int kbase = tile_of(j) * kBlockN;
       const bool need_mask = (kbase + kBlockN > kv_lim) || (causal && kbase + kBlockN - 1 > q0) || a.bits;
-      if (need_mask) {
-        int lim = kv_lim - kbase;
-        if (causal) lim = min(lim, row + 1 - kbase);
-        uint32_t wbits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
-        if (a.bits && row < a.Sq) {
-          const uint32_t* br = a.bits + (static_cast<int64_t>(b) * a.Sq + row) * bit_words;
+      // First pass: exponentials against the running max as it stands.  That
+      // is exactly the result of the rescale rule below whenever no score of
+      // the tile exceeds the running max by more than kRescaleThreshold, and
+      // a tile row sum <= 2^kRescaleThreshold proves that.  Otherwise (and on
+      // a row's first tile) a second pass reloads the scores, takes the row
+      // max, rescales if it grew past the threshold and recomputes.  The pass
+      // decision is per warp: tensor-memory loads are warp-collective.
+      bool with_max = __any_sync(0xFFFFFFFFu, m_ref == -INFINITY);
+      float tile_sum = 0.0f;
+      uint32_t pr[2][32];
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        uint32_t sr[4][32];
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int64_t wi = kbase / 32 + w;
-            wbits[w] = wi < bit_words ? br[wi] : 0u;
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        if (t == 0) H3_TRACE(kEvSmLd0, j);
+        float s[kBlockN];
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+        if (need_mask) {
+          int lim = kv_lim - kbase;
+          if (causal) lim = min(lim, row + 1 - kbase);
+          uint32_t wbits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+          if (a.bits && row < a.Sq) {
+            const uint32_t* br = a.bits + (static_cast<int64_t>(b) * a.Sq + row) * bit_words;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int64_t wi = kbase / 32 + w;
+              wbits[w] = wi < bit_words ? br[wi] : 0u;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c) {
+            const bool allowed = (c < lim) && ((wbits[c >> 5] >> (c & 31)) & 1u);
+            s[c] = allowed ? s[c] : -INFINITY;
           }
         }
+        if (with_max) {
+          // row max: 3-input max in 8 independent chains
+          float mx[8];
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c) {
-          const bool allowed = (c < lim) && ((wbits[c >> 5] >> (c & 31)) & 1u);
-          s[c] = allowed ? s[c] : -INFINITY;
-        }
-      }
-      // row max: 3-input max in 8 independent chains
-      float mx[8];
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+          for (int c = 16; c < kBlockN; c += 16) {
 #pragma unroll
-      for (int c = 16; c < kBlockN; c += 16) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
-      }
-      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
-      const float mt_s = mt * sl;
-      const bool grow = mt_s > m_ref + kRescaleThreshold;
-      float alpha = 1.0f;
-      if (grow) {
-        alpha = ex2(m_ref - mt_s);  // m_ref = -inf gives 0
-        l *= alpha;
-        m_ref = mt_s;
-      }
-      if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
-        // O must hold every P V product of tiles < j before it is rescaled;
-        // the products are sequential, so the last one completing is enough.
-        ok = wait_pv(j - 1);
-        if (!__all_sync(0xFFFFFFFFu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+            for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+          }
+          const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+          const float mt_s = mt * sl;
+          const bool grow = mt_s > m_ref + kRescaleThreshold;
+          float alpha = 1.0f;
+          if (grow) {
+            alpha = ex2(m_ref - mt_s);  // m_ref = -inf gives 0
+            l *= alpha;
+            m_ref = mt_s;
+          }
+          if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
+            // O must hold every P V product of tiles < j before it is
+            // rescaled; the products are sequential, so the last one
+            // completing is enough.
+            ok = wait_pv(j - 1);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait(o);
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c * 32, o);
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + c * 32, o);
+            }
+            tmem_st_wait();
+          }
         }
-        tmem_st_wait();
-      }
-      const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
-      // p = exp2(s * scale*log2e - m): packed FMA, ex2, packed row-sum
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pr[2][32];
+        const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
+        // p = exp2(s * scale*log2e - m): packed FMA, ex2, packed row-sum
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kBlockN; c += 2) {
-        float t0, t1;
-        ffma2(t0, t1, s[c], s[c + 1], sl, sl, -mu, -mu);
-        const float p0 = ex2(t0);
-        const float p1 = ex2(t1);
-        const int a2 = ((c >> 1) & 3) * 2;
-        fadd2(ls[a2], ls[a2 + 1], ls[a2], ls[a2 + 1], p0, p1);
-        pr[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < kBlockN; c += 2) {
+          float t0, t1;
+          ffma2(t0, t1, s[c], s[c + 1], sl, sl, -mu, -mu);
+          const float p0 = ex2(t0);
+          const float p1 = ex2(t1);
+          const int a2 = ((c >> 1) & 3) * 2;
+          fadd2(ls[a2], ls[a2 + 1], ls[a2], ls[a2 + 1], p0, p1);
+          pr[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
+        }
+        tile_sum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        if (with_max) break;
+        with_max = __any_sync(0xFFFFFFFFu, !(tile_sum <= kFastPassSumLimit));
+        if (!with_max) break;
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      if (!ok) break;
+      l += tile_sum;
       if (t == 0) H3_TRACE(kEvSmExp0, j);
+      tc_fence_before();
+      mbar_arrive(bar_s_read(j & 1));  // S_{j mod 2} may be overwritten by S_{j+2}
       // The single P buffer is free once O += P_{j-1} V_{j-1} has completed.
       if (j > 0) {
         ok = wait_pv(j - 1);
