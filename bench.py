@@ -367,9 +367,9 @@ def run_gpu(args):
 
 
 # The library's choice of attention kernel: one query tile per CTA (Q held in
-# tensor memory) from 8192 keys on, for head dims 64 and 128; two query tiles
+# tensor memory) from 1024 keys on, for head dims 64 and 128; two query tiles
 # per CTA otherwise.  H3ATTN_ATTN_KERNEL=1/2 forces one or the other.
-ONE_TILE_MIN_KEYS = 8192
+ONE_TILE_MIN_KEYS = 1024
 
 
 def _attn_kernel_name(wl):

@@ -499,10 +499,10 @@ int read_and_clear_status(int* value) {
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   // Two kernels for head_dim 64/128: one query tile per CTA with Q in tensor
-  // memory (faster when there are many key tiles to amortise its longer
-  // per-tile chain), or two query tiles per CTA sharing each K/V tile
-  // (faster on short key ranges).  a.kernel: 0 = by key length, 1 = one
-  // query tile, 2 = two query tiles.
+  // memory and two MMA-issuing threads (faster from about a thousand keys
+  // on), or two query tiles per CTA sharing each K/V tile (faster on short
+  // key ranges, where its shorter prologue matters).  a.kernel: 0 = by key
+  // length, 1 = one query tile, 2 = two query tiles.
   const bool one_tile = a.kernel == 1 || (a.kernel == 0 && a.Sk >= kOneTileMinKeys);
   switch (a.D) {
     case 64: return one_tile ? launch_pipe<64, 12>(a, stream) : launch_cfg<64, 2, 8>(a, stream);

@@ -68,7 +68,7 @@ struct AttnArgs {
   int kernel;               // 0 = choose by key length, 1 = one query tile per CTA, 2 = two
 };
 // Key length from which the one-query-tile kernel is chosen (head_dim 64/128).
-constexpr int kOneTileMinKeys = 8192;
+constexpr int kOneTileMinKeys = 1024;
 // Box rows of the Q/K/V maps built by the launcher.
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
