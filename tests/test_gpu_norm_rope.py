@@ -60,6 +60,12 @@ def test_bit_exact_cross_attention_query_only(h3):
     (64, 64, 0.0, 1, 31, 2, 2),
     (256, 96, 1e-6, 2, 29, 2, 2),
     (256, 256, 1e-6, 1, 17, 3, 3),
+    # table rows staged with the chunk, chunks crossing sample boundaries
+    (128, 96, 1e-6, 3, 5, 24, 12),
+    (64, 64, 1e-6, 2, 9, 20, 20),
+    (256, 128, 1e-6, 2, 7, 12, 12),
+    # chunks spanning more tokens than a sample has positions: tables read directly
+    (128, 96, 1e-6, 4, 2, 16, 8),
 ])
 def test_bit_exact_edge_shapes(h3, D, rot, eps, B, S, Hq, Hkv):
     q = gen.normal_bshd(B, S, Hq, D, 7, gen.STREAM_Q, 2.0, 0.5)

@@ -35,7 +35,8 @@ namespace h3 {
 namespace {
 
 constexpr int kComputeWarps = 8;
-constexpr int kStages = 4;
+constexpr int kStages = 3;     // row stages
+constexpr int kTabSlots = 6;   // RoPE table slots, released later than the rows
 constexpr int kNormThreads = (kComputeWarps + 1) * 32;  // + one producer warp
 constexpr int kChunkBytes = 16384;
 constexpr int kUnroll = 4;  // rows per lane slot per chunk; also rows sharing one sqrt/div pass
@@ -46,7 +47,15 @@ struct NormCfg {
   static constexpr int RPW = 32 / LPR;                      // rows per warp per access
   static constexpr int kRows = kChunkBytes / (D * 2);       // rows per chunk
   static_assert(kRows == kComputeWarps * RPW * kUnroll, "chunk = compute warps x rows per warp");
-  static constexpr int kSmem = kStages * kChunkBytes + 2 * kStages * 8 + 16;
+  // Tokens whose RoPE table rows a slot holds: a chunk of kRows rows spans at
+  // most 8 tokens once a token has kRows / 7 heads or more.
+  static constexpr int kTabTokens = D == 256 ? 4 : 8;
+  static constexpr int kTabBytes = kTabTokens * (D / 2) * 4;  // one table, rows of at most D/2 floats
+  static constexpr int kSlotBytes = 2 * kTabBytes;            // cos rows, then sin rows
+  static constexpr int kTabBase = kStages * kChunkBytes;
+  static constexpr int kBarBase = kTabBase + kTabSlots * kSlotBytes;
+  // full[kStages], empty[kStages], tab_empty[kTabSlots]
+  static constexpr int kSmem = kBarBase + (2 * kStages + kTabSlots) * 8 + 16;
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -77,10 +86,11 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
   static_assert(LPR >= U, "each row needs a lane per unrolled row for the shared sqrt/div pass");
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bars = sbase + kStages * kChunkBytes;
+  const uint32_t bars = sbase + C::kBarBase;
   auto bar_full = [&](int st) { return bars + 8u * st; };
   auto bar_empty = [&](int st) { return bars + 8u * (kStages + st); };
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kStages * kChunkBytes + 2 * kStages * 8);
+  auto bar_tab_empty = [&](int ts) { return bars + 8u * (2 * kStages + ts); };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kBarBase + (2 * kStages + kTabSlots) * 8);
   WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
 
   const int warp = threadIdx.x >> 5;
@@ -90,6 +100,7 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
       mbar_init(bar_full(st), 1);
       mbar_init(bar_empty(st), kComputeWarps);
     }
+    for (int ts = 0; ts < kTabSlots; ++ts) mbar_init(bar_tab_empty(ts), kComputeWarps);
     *abort_flag = 0u;
     fence_barrier_init();
   }
@@ -97,6 +108,15 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
 
   const uint32_t n_q_chunks = (a.rows_q + C::kRows - 1) / C::kRows;
   const uint32_t n_chunks = n_q_chunks + (a.rows_k + C::kRows - 1) / C::kRows;
+  const int half = a.rotary_dim >> 1;
+  // Tokens [tok0, tok0 + ntok) of a chunk; their table rows are staged with
+  // the chunk when they fit and ntok <= S, so that their positions form at
+  // most two runs (tok0 and ntok are recomputed by both sides).
+  auto chunk_tokens = [&](bool is_q, uint32_t row0, uint32_t nrows, uint32_t& tok0, uint32_t& ntok) {
+    const FastDiv& dh = is_q ? a.div_hq : a.div_hkv;
+    tok0 = fdiv(row0, dh);
+    ntok = fdiv(row0 + nrows - 1, dh) - tok0 + 1;
+  };
 
   if (warp == kComputeWarps) {
     // ---------------- producer: chunk -> shared-memory stage ----------------
@@ -104,13 +124,33 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
       uint32_t it = 0;
       for (uint32_t c = blockIdx.x; c < n_chunks; c += gridDim.x, ++it) {
         const int st = it % kStages;
+        const int ts = it % kTabSlots;
         if (!mbar_wait(bar_empty(st), ((it / kStages) & 1) ^ 1u, ctl)) break;
+        if (!mbar_wait(bar_tab_empty(ts), ((it / kTabSlots) & 1) ^ 1u, ctl)) break;
         bool is_q;
         uint32_t row0, nrows;
         chunk_of(a, c, C::kRows, n_q_chunks, is_q, row0, nrows);
         const uint16_t* src = (is_q ? a.q : a.k) + static_cast<size_t>(row0) * D;
-        mbar_arrive_expect_tx(bar_full(st), nrows * D * 2);
-        bulk_load(sbase + st * kChunkBytes, src, nrows * D * 2, bar_full(st));
+        uint32_t tok0, ntok;
+        chunk_tokens(is_q, row0, nrows, tok0, ntok);
+        const bool staged = half > 0 && ntok <= static_cast<uint32_t>(C::kTabTokens) && ntok <= a.div_s.d;
+        const uint32_t tab_bytes = staged ? ntok * half * 4 : 0u;
+        const uint32_t stage = sbase + st * kChunkBytes;
+        const uint32_t slot_c = sbase + C::kTabBase + ts * C::kSlotBytes;  // cos rows; sin rows follow
+        mbar_arrive_expect_tx(bar_full(st), nrows * D * 2 + 2 * tab_bytes);
+        bulk_load(stage, src, nrows * D * 2, bar_full(st));
+        if (staged) {
+          // positions tok % S: one run, or two when the chunk crosses a sample boundary
+          const uint32_t pos0 = tok0 - fdiv(tok0, a.div_s) * a.div_s.d;
+          const uint32_t n1 = min(ntok, a.div_s.d - pos0);
+          const uint32_t b1 = n1 * half * 4;
+          bulk_load(slot_c, a.cos + static_cast<size_t>(pos0) * half, b1, bar_full(st));
+          bulk_load(slot_c + C::kTabBytes, a.sin + static_cast<size_t>(pos0) * half, b1, bar_full(st));
+          if (n1 < ntok) {
+            bulk_load(slot_c + b1, a.cos, tab_bytes - b1, bar_full(st));
+            bulk_load(slot_c + C::kTabBytes + b1, a.sin, tab_bytes - b1, bar_full(st));
+          }
+        }
       }
       // every issued copy has landed before the CTA retires
       const uint32_t first = it > kStages ? it - kStages : 0;
@@ -127,7 +167,6 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
   const uint32_t lr = lane % LPR;  // lane within its row
   const uint32_t slot = lane / LPR;
   const uint32_t row_lane0 = lane - lr;
-  const int half = a.rotary_dim >> 1;
   const uint32_t hl = static_cast<uint32_t>(half >> 3);  // lanes per rotated half
   const bool rotating = lr < 2 * hl;
   // Rotation partner: lanes [0, hl) pair with [hl, 2hl) of the same row.
@@ -144,6 +183,12 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
     uint32_t row0, nrows;
     chunk_of(a, c, C::kRows, n_q_chunks, is_q, row0, nrows);
     const uint8_t* stage = smem + st * kChunkBytes;
+    const int ts = it % kTabSlots;
+    const float* tab_c = reinterpret_cast<const float*>(smem + C::kTabBase + ts * C::kSlotBytes);
+    const float* tab_s = tab_c + C::kTabBytes / 4;
+    uint32_t tok0, ntok;
+    chunk_tokens(is_q, row0, nrows, tok0, ntok);
+    const bool staged = half > 0 && ntok <= static_cast<uint32_t>(C::kTabTokens) && ntok <= a.div_s.d;
 
     uint4 xv[U];
     uint32_t lrow[U];
@@ -212,13 +257,23 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
       uint32_t ob[4] = {nb[0], nb[1], nb[2], nb[3]};
       if (rotating) {
         const uint32_t tok = fdiv(r, dh);
-        const uint32_t pos = tok - fdiv(tok, a.div_s) * a.div_s.d;
-        const float* ct = a.cos + static_cast<size_t>(pos) * half + ti;
-        const float* stb = a.sin + static_cast<size_t>(pos) * half + ti;
-        const float4 c0 = __ldg(reinterpret_cast<const float4*>(ct));
-        const float4 c1 = __ldg(reinterpret_cast<const float4*>(ct + 4));
-        const float4 s0 = __ldg(reinterpret_cast<const float4*>(stb));
-        const float4 s1 = __ldg(reinterpret_cast<const float4*>(stb + 4));
+        float4 c0, c1, s0, s1;
+        if (staged) {
+          const float* ct = tab_c + (tok - tok0) * half + ti;
+          const float* stb = tab_s + (tok - tok0) * half + ti;
+          c0 = *reinterpret_cast<const float4*>(ct);
+          c1 = *reinterpret_cast<const float4*>(ct + 4);
+          s0 = *reinterpret_cast<const float4*>(stb);
+          s1 = *reinterpret_cast<const float4*>(stb + 4);
+        } else {
+          const uint32_t pos = tok - fdiv(tok, a.div_s) * a.div_s.d;
+          const float* ct = a.cos + static_cast<size_t>(pos) * half + ti;
+          const float* stb = a.sin + static_cast<size_t>(pos) * half + ti;
+          c0 = __ldg(reinterpret_cast<const float4*>(ct));
+          c1 = __ldg(reinterpret_cast<const float4*>(ct + 4));
+          s0 = __ldg(reinterpret_cast<const float4*>(stb));
+          s1 = __ldg(reinterpret_cast<const float4*>(stb + 4));
+        }
         const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         // sine with this lane's sign folded in: (-s) * b == -(b * s) exactly
         const float sv[8] = {__uint_as_float(__float_as_uint(s0.x) ^ neg), __uint_as_float(__float_as_uint(s0.y) ^ neg),
@@ -235,6 +290,8 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
       }
       *reinterpret_cast<uint4*>(gbase + static_cast<size_t>(r) * D + lr * 8) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_tab_empty(ts));  // this warp is done with the table slot
   }
 }
 
