@@ -112,6 +112,25 @@ h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const flo
                                     h3attn_stream_t stream);
 
 /*
+ * The same fused Q/K RMSNorm -> bf16 boundary -> partial RoPE, written to
+ * separate output tensors so that the raw q and k stay available (SGLang PR
+ * #37903 "[diffusion] model: support VDN-H3 ...", section "Modifications",
+ * hybrid attention module: an out-of-place fused QK-norm + RoPE, bit-equal to
+ * the in-place one, lets the linear branch keep the raw q/k).  Every output
+ * element is bit-identical to what h3attn_qk_norm_rope() writes in place.
+ *
+ * q, k: inputs as above (device, read only); q_out: [B, S, Hq, D] and
+ *    k_out: [B, S, Hkv, D] bf16 outputs (device), present exactly when the
+ *    matching input is.  An output may be its own input (then the call is the
+ *    in-place one); any other overlap among q, k, q_out, k_out is rejected.
+ * Other arguments, alignment and errors as for h3attn_qk_norm_rope().
+ */
+h3attn_status_t h3attn_qk_norm_rope_out(const void* q, const void* k, void* q_out, void* k_out,
+                                        const float* wq, const float* wk, const float* cos,
+                                        const float* sin, int B, int S, int Hq, int Hkv, int D,
+                                        int rotary_dim, float eps, h3attn_stream_t stream);
+
+/*
  * Dense prefill attention  o = softmax(q k^T * scale) v  per (batch, query
  * head), on BSHD bf16 tensors (FastVideo PR #1832, section "Summary": dense
  * non-causal self-attention with head_dim 128; FastVideo PR #1799, section

@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("h3attn_qk_norm_rope", "h3attn_prefill", "h3attn_status_string",
+    for n in ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_status_string",
               "h3attn_check_device_status", "h3attn_version"):
         assert n in names
     assert set(names) == set(h3.EXPORTED)
@@ -97,3 +97,22 @@ def test_norm_rope_validation(lib):
     assert norm(lib, k=FAKE + 256) == h3.H3ATTN_ERR_INVALID_ARG  # k overlaps q
     assert norm(lib, B=0) == h3.H3ATTN_OK
     assert norm(lib, q=None, Hq=0, k=None, Hkv=0) == h3.H3ATTN_OK
+
+
+def norm_out(lib, q=FAKE, k=FAKE * 64, q_out=FAKE * 400, k_out=FAKE * 500, wq=FAKE * 200, wk=FAKE * 201,
+             cos=FAKE * 202, sin=FAKE * 203, B=1, S=16, Hq=2, Hkv=2, D=128, rot=96, eps=1e-6):
+    return lib.h3attn_qk_norm_rope_out(q, k, q_out, k_out, wq, wk, cos, sin, B, S, Hq, Hkv, D, rot, eps, None)
+
+
+def test_norm_rope_out_validation(lib):
+    rows_bytes = 16 * 2 * 128 * 2  # one tensor of B*S*H rows of D bf16
+    assert norm_out(lib, q_out=None) == h3.H3ATTN_ERR_INVALID_ARG          # output missing
+    assert norm_out(lib, q=None, Hq=0) == h3.H3ATTN_ERR_INVALID_ARG        # output without input
+    assert norm_out(lib, q_out=FAKE * 400 + 8) == h3.H3ATTN_ERR_MISALIGNED
+    assert norm_out(lib, q_out=FAKE + rows_bytes // 2) == h3.H3ATTN_ERR_INVALID_ARG   # partly over q
+    assert norm_out(lib, q_out=FAKE * 64) == h3.H3ATTN_ERR_INVALID_ARG      # writes over input k
+    assert norm_out(lib, k_out=FAKE) == h3.H3ATTN_ERR_INVALID_ARG           # writes over input q
+    assert norm_out(lib, k_out=FAKE * 400 + 256) == h3.H3ATTN_ERR_INVALID_ARG  # overlaps q_out
+    assert norm_out(lib, D=80) == h3.H3ATTN_ERR_UNSUPPORTED_HEAD_DIM
+    assert norm_out(lib, B=0) == h3.H3ATTN_OK
+    assert norm_out(lib, q=None, Hq=0, q_out=None, k=None, Hkv=0, k_out=None) == h3.H3ATTN_OK

@@ -91,3 +91,55 @@ def test_zero_rows_and_tiny_values(h3):
     gq, gk = _run(h3, q, k, w, w, cos, sin, 96, 1e-6)
     _assert_bits_equal(gq, oracle.qk_norm_rope_emulate(q, w, cos, sin, 96, 1e-6), "q")
     _assert_bits_equal(gk, oracle.qk_norm_rope_emulate(k, w, cos, sin, 96, 1e-6), "k")
+
+
+# ---------------------------------------------------------------- out of place
+def _run_out(h3, q_bits, k_bits, wq, wk, cos, sin, rot, eps, alias=False):
+    import torch
+    q, k = to_dev(q_bits), to_dev(k_bits)
+    q_out = q if alias else torch.full_like(q, float("nan"))
+    k_out = k if alias else torch.full_like(k, float("nan"))
+    h3.h3attn_qk_norm_rope_out(q, k, q_out, k_out, to_dev_f32(wq), to_dev_f32(wk),
+                               to_dev_f32(cos) if cos is not None else None,
+                               to_dev_f32(sin) if sin is not None else None, rot, eps)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    return from_dev(q), from_dev(k), from_dev(q_out), from_dev(k_out)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["tiny_mha", "dit_block", "padded_gqa"])
+def test_out_of_place_bit_equal_and_inputs_kept(h3, name):
+    wl = gen.WORKLOADS[name]
+    inp = gen.make_inputs(wl, seed=1234)
+    gq, gk, oq, ok_ = _run_out(h3, inp.q, inp.k, inp.wq, inp.wk, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+    # the raw inputs are untouched
+    _assert_bits_equal(gq, inp.q, f"{name} q input")
+    _assert_bits_equal(gk, inp.k, f"{name} k input")
+    # the outputs equal the emulation and the in-place kernel bit for bit
+    eq = oracle.qk_norm_rope_emulate(inp.q, inp.wq, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+    ek = oracle.qk_norm_rope_emulate(inp.k, inp.wk, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+    _assert_bits_equal(oq, eq, f"{name} q_out")
+    _assert_bits_equal(ok_, ek, f"{name} k_out")
+    iq, ik = _run(h3, inp.q, inp.k, inp.wq, inp.wk, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
+    _assert_bits_equal(oq, iq, f"{name} q_out vs in place")
+    _assert_bits_equal(ok_, ik, f"{name} k_out vs in place")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,rot,B,S,Hq,Hkv", [(128, 96, 2, 37, 3, 1), (64, 32, 3, 9, 20, 4), (256, 128, 1, 17, 3, 3)])
+def test_out_of_place_edge_shapes_and_alias(h3, D, rot, B, S, Hq, Hkv):
+    q = gen.normal_bshd(B, S, Hq, D, 11, gen.STREAM_Q)
+    k = gen.normal_bshd(B, S, Hkv, D, 11, gen.STREAM_K)
+    w = gen.uniform_f32(D, 11, gen.STREAM_WQ, 0.5, 1.5)
+    cos, sin = gen.rope_tables(S, rot)
+    eq = oracle.qk_norm_rope_emulate(q, w, cos, sin, rot, 1e-6)
+    ek = oracle.qk_norm_rope_emulate(k, w, cos, sin, rot, 1e-6)
+    gq, gk, oq, ok_ = _run_out(h3, q, k, w, w, cos, sin, rot, 1e-6)
+    _assert_bits_equal(gq, q, "q input kept")
+    _assert_bits_equal(oq, eq, "q_out")
+    _assert_bits_equal(ok_, ek, "k_out")
+    # outputs that are their own inputs: the in-place call
+    gq, gk, _, _ = _run_out(h3, q, k, w, w, cos, sin, rot, 1e-6, alias=True)
+    _assert_bits_equal(gq, eq, "aliased q")
+    _assert_bits_equal(gk, ek, "aliased k")

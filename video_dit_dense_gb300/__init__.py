@@ -5,12 +5,16 @@ kernels of ``libh3attn.so``.  PyTorch supplies device memory and streams.
 There is no CPU or eager fallback: if the library is missing or the device
 is not sm_103, calls raise.
 
-The two entry points mirror the C ABI in ``include/h3attn.h``:
+The entry points mirror the C ABI in ``include/h3attn.h``:
 
 * ``h3attn_qk_norm_rope(q, k, wq, wk, cos, sin, rotary_dim, eps, stream)`` --
   fused Q/K RMSNorm, bf16 boundary and partial RoPE, in place (FastVideo
   PR #1832 "Add FlashInfer attention backend support for MiniMax H3",
   section "Preserve H3-specific attention behavior").
+* ``h3attn_qk_norm_rope_out(q, k, q_out, k_out, ...)`` -- the same step into
+  separate outputs, leaving the raw q and k in place (SGLang PR #37903
+  "[diffusion] model: support VDN-H3 ...", section "Modifications": the
+  out-of-place variant, bit-equal to the in-place one, keeps the raw q/k).
 * ``h3attn_prefill(q, k, v, o, scale, mask, causal, stream)`` -- dense
   prefill attention on BSHD bf16 tensors with GQA, cross-attention, causal
   and boolean-mask variants (FastVideo PR #1799 "Add opt-in FlashInfer
@@ -36,7 +40,7 @@ H3ATTN_ERR_LAUNCH = 6
 H3ATTN_ERR_TIMEOUT = 7
 
 # Every symbol include/h3attn.h declares.
-EXPORTED = ("h3attn_qk_norm_rope", "h3attn_prefill", "h3attn_status_string",
+EXPORTED = ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_status_string",
             "h3attn_check_device_status", "h3attn_version")
 
 
@@ -73,6 +77,8 @@ def load(path: str = LIB_PATH):
             P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             lib.h3attn_qk_norm_rope.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, P]
             lib.h3attn_qk_norm_rope.restype = I
+            lib.h3attn_qk_norm_rope_out.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+            lib.h3attn_qk_norm_rope_out.restype = I
             lib.h3attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, F,
                                            ctypes.POINTER(h3attn_mask_t), I, P]
             lib.h3attn_prefill.restype = I
@@ -116,13 +122,7 @@ def _raise_if(status, where):
         raise H3AttnError(status, where)
 
 
-def h3attn_qk_norm_rope(q, k, wq, wk, cos, sin, rotary_dim=96, eps=1e-6, stream=None):
-    """In-place fused Q/K RMSNorm + bf16 boundary + partial RoPE.
-
-    q: [B, S, Hq, D] bf16, k: [B, S, Hkv, D] bf16 (either may be None);
-    wq, wk: [D] float32; cos, sin: [>=S, rotary_dim/2] float32.
-    """
-    load()
+def _norm_rope_args(q, k, wq, wk, cos, sin, rotary_dim):
     ref = q if q is not None else k
     if q is not None:
         _check_bf16("q", q)
@@ -140,9 +140,40 @@ def h3attn_qk_norm_rope(q, k, wq, wk, cos, sin, rotary_dim=96, eps=1e-6, stream=
     if rotary_dim > 0 and (cos.shape[-1] != rotary_dim // 2 or cos.numel() < S * (rotary_dim // 2)
                            or sin.shape != cos.shape):
         raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "cos/sin must be [>=S, rotary_dim/2]")
+    return B, S, Hq, Hkv, D
+
+
+def h3attn_qk_norm_rope(q, k, wq, wk, cos, sin, rotary_dim=96, eps=1e-6, stream=None):
+    """In-place fused Q/K RMSNorm + bf16 boundary + partial RoPE.
+
+    q: [B, S, Hq, D] bf16, k: [B, S, Hkv, D] bf16 (either may be None);
+    wq, wk: [D] float32; cos, sin: [>=S, rotary_dim/2] float32.
+    """
+    load()
+    B, S, Hq, Hkv, D = _norm_rope_args(q, k, wq, wk, cos, sin, rotary_dim)
     st = _lib.h3attn_qk_norm_rope(_ptr(q), _ptr(k), _ptr(wq), _ptr(wk), _ptr(cos), _ptr(sin),
                                   B, S, Hq, Hkv, D, int(rotary_dim), float(eps), _stream_handle(stream))
     _raise_if(st, "h3attn_qk_norm_rope")
+
+
+def h3attn_qk_norm_rope_out(q, k, q_out, k_out, wq, wk, cos, sin, rotary_dim=96, eps=1e-6, stream=None):
+    """Out-of-place fused Q/K RMSNorm + bf16 boundary + partial RoPE: q and k
+    are read only; q_out, k_out (same shapes, preallocated) receive the
+    result, bit-identical to the in-place call."""
+    load()
+    B, S, Hq, Hkv, D = _norm_rope_args(q, k, wq, wk, cos, sin, rotary_dim)
+    for name, src, dst in (("q_out", q, q_out), ("k_out", k, k_out)):
+        if (src is None) != (dst is None):
+            raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must be given exactly when its input is")
+        if dst is not None:
+            _check_bf16(name, dst)
+            if tuple(dst.shape) != tuple(src.shape):
+                raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must have the shape of its input")
+    st = _lib.h3attn_qk_norm_rope_out(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(wq), _ptr(wk), _ptr(cos),
+                                      _ptr(sin), B, S, Hq, Hkv, D, int(rotary_dim), float(eps),
+                                      _stream_handle(stream))
+    _raise_if(st, "h3attn_qk_norm_rope_out")
+    return q_out, k_out
 
 
 @dataclass

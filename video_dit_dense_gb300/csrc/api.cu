@@ -101,15 +101,22 @@ const char* h3attn_status_string(h3attn_status_t s) {
   return "unknown status";
 }
 
-h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const float* wk,
-                                    const float* cos, const float* sin, int B, int S, int Hq,
-                                    int Hkv, int D, int rotary_dim, float eps,
-                                    h3attn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of the in-place and out-of-place norm/RoPE entry points.  An
+// output may be its own input (in place); any other overlap between the four
+// row tensors is rejected.
+h3attn_status_t norm_rope(const void* q, const void* k, void* q_out, void* k_out, const float* wq,
+                          const float* wk, const float* cos, const float* sin, int B, int S, int Hq, int Hkv,
+                          int D, int rotary_dim, float eps, h3attn_stream_t stream) {
   if (B < 0 || S < 0 || Hq < 0 || Hkv < 0) return H3ATTN_ERR_INVALID_ARG;
   if (!head_dim_ok(D)) return H3ATTN_ERR_UNSUPPORTED_HEAD_DIM;
   if (rotary_dim < 0 || rotary_dim > D || rotary_dim % 16 != 0) return H3ATTN_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || !isfinite(eps)) return H3ATTN_ERR_INVALID_ARG;
   if ((q == nullptr) != (Hq == 0) || (k == nullptr) != (Hkv == 0)) return H3ATTN_ERR_INVALID_ARG;
+  if ((q_out == nullptr) != (q == nullptr) || (k_out == nullptr) != (k == nullptr)) return H3ATTN_ERR_INVALID_ARG;
   if (q && !wq) return H3ATTN_ERR_INVALID_ARG;
   if (k && !wk) return H3ATTN_ERR_INVALID_ARG;
   if (rotary_dim > 0 && (!cos || !sin)) return H3ATTN_ERR_INVALID_ARG;
@@ -117,15 +124,22 @@ h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const flo
   const int64_t rows_k = static_cast<int64_t>(B) * S * Hkv;
   if (rows_q + rows_k == 0) return H3ATTN_OK;
   if (rows_q + rows_k >= (1LL << 31)) return H3ATTN_ERR_INVALID_ARG;
-  if ((q && !aligned16(q)) || (k && !aligned16(k)) || (wq && !aligned16(wq)) ||
-      (wk && !aligned16(wk)) || (cos && !aligned16(cos)) || (sin && !aligned16(sin)))
+  if ((q && !aligned16(q)) || (k && !aligned16(k)) || (q_out && !aligned16(q_out)) || (k_out && !aligned16(k_out)) ||
+      (wq && !aligned16(wq)) || (wk && !aligned16(wk)) || (cos && !aligned16(cos)) || (sin && !aligned16(sin)))
     return H3ATTN_ERR_MISALIGNED;
-  if (q && k && overlap(q, rows_q * D * 2, k, rows_k * D * 2)) return H3ATTN_ERR_INVALID_ARG;
+  const int64_t nq = rows_q * D * 2, nk = rows_k * D * 2;
+  if (q && k && overlap(q, nq, k, nk)) return H3ATTN_ERR_INVALID_ARG;
+  if (q && k && (overlap(q_out, nq, k, nk) || overlap(q_out, nq, k_out, nk) || overlap(k_out, nk, q, nq)))
+    return H3ATTN_ERR_INVALID_ARG;
+  if (q && q_out != q && overlap(q_out, nq, q, nq)) return H3ATTN_ERR_INVALID_ARG;
+  if (k && k_out != k && overlap(k_out, nk, k, nk)) return H3ATTN_ERR_INVALID_ARG;
   h3attn_status_t st = check_device();
   if (st != H3ATTN_OK) return st;
   h3::NormRopeArgs a;
-  a.q = static_cast<uint16_t*>(q);
-  a.k = static_cast<uint16_t*>(k);
+  a.q_in = static_cast<const uint16_t*>(q);
+  a.k_in = static_cast<const uint16_t*>(k);
+  a.q_out = static_cast<uint16_t*>(q_out);
+  a.k_out = static_cast<uint16_t*>(k_out);
   a.wq = wq;
   a.wk = wk;
   a.cos = cos;
@@ -143,6 +157,24 @@ h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const flo
   a.wait_limit_ns = wait_limit_ns();
   cudaError_t e = h3::launch_qk_norm_rope(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+h3attn_status_t h3attn_qk_norm_rope(void* q, void* k, const float* wq, const float* wk,
+                                    const float* cos, const float* sin, int B, int S, int Hq,
+                                    int Hkv, int D, int rotary_dim, float eps,
+                                    h3attn_stream_t stream) {
+  return norm_rope(q, k, q, k, wq, wk, cos, sin, B, S, Hq, Hkv, D, rotary_dim, eps, stream);
+}
+
+h3attn_status_t h3attn_qk_norm_rope_out(const void* q, const void* k, void* q_out, void* k_out,
+                                        const float* wq, const float* wk, const float* cos,
+                                        const float* sin, int B, int S, int Hq, int Hkv, int D,
+                                        int rotary_dim, float eps, h3attn_stream_t stream) {
+  return norm_rope(q, k, q_out, k_out, wq, wk, cos, sin, B, S, Hq, Hkv, D, rotary_dim, eps, stream);
 }
 
 h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Sq,

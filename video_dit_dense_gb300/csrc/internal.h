@@ -35,8 +35,10 @@ inline FastDiv make_fastdiv(uint32_t d) {
 }
 
 struct NormRopeArgs {
-  uint16_t* q;
-  uint16_t* k;
+  const uint16_t* q_in;   // rows read (== q_out / k_out for the in-place call)
+  const uint16_t* k_in;
+  uint16_t* q_out;        // rows written
+  uint16_t* k_out;
   const float* wq;
   const float* wk;
   const float* cos;

@@ -1,4 +1,5 @@
-// Fused Q/K RMSNorm -> bf16 boundary -> partial rotate-half RoPE, in place.
+// Fused Q/K RMSNorm -> bf16 boundary -> partial rotate-half RoPE, in place or
+// into separate output tensors.
 //
 // The step MiniMax-H3 runs on Q and K before attention (FastVideo PR #1832
 // "Add FlashInfer attention backend support for MiniMax H3", section
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
         bool is_q;
         uint32_t row0, nrows;
         chunk_of(a, c, C::kRows, n_q_chunks, is_q, row0, nrows);
-        const uint16_t* src = (is_q ? a.q : a.k) + static_cast<size_t>(row0) * D;
+        const uint16_t* src = (is_q ? a.q_in : a.k_in) + static_cast<size_t>(row0) * D;
         uint32_t tok0, ntok;
         chunk_tokens(is_q, row0, nrows, tok0, ntok);
         const bool staged = half > 0 && ntok <= static_cast<uint32_t>(C::kTabTokens) && ntok <= a.div_s.d;
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
     const float4 w1 = __ldg(reinterpret_cast<const float4*>(wp + 4));
     const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     const FastDiv& dh = is_q ? a.div_hq : a.div_hkv;
-    uint16_t* gbase = is_q ? a.q : a.k;
+    uint16_t* gbase = is_q ? a.q_out : a.k_out;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
