@@ -15,6 +15,11 @@ What it computes (all in double precision, from the definitions):
 * ``qk_norm_rope_emulate`` -- the same step in float32 in a fixed operation
   order; the bit-exact contract for the CUDA norm/RoPE kernel (TeleFuser
   PR #37 section 2.5 holds fused kernels to element-wise bit-exactness).
+* ``rmsnorm_modulate_f64`` / ``rmsnorm_modulate_emulate`` -- RMSNorm of a DiT
+  hidden row, then indexed AdaLN modulation y = n * (1 + scale[idx]) +
+  shift[idx] with the bf16 store after every step of the unfused path
+  (TeleFuser PR #37 section 2.5); fp64 definition and the float32
+  fixed-order contract of the CUDA kernel.
 * ``attention_f64`` -- softmax(Q K^T * scale) V per output row with GQA,
   cross-attention, causal, key-padding and packed boolean [Q, K] masks
   (FastVideo PR #1799 "Add opt-in FlashInfer attention backend for Wan",
@@ -76,6 +81,10 @@ def _load():
             lib.oracle_attention_f64.argtypes = [P, P, P, I, I, I, I, I, I, D, I, P, P, P, P, P,
                                                  I64, P, I]
             lib.oracle_round_f64_to_bf16.argtypes = [P, P, I64]
+            lib.oracle_rmsnorm_modulate_f64.argtypes = [P, P, I64, I, P, P, P, P, I, D, I]
+            lib.oracle_rmsnorm_modulate_emulate_bf16.argtypes = [P, P, I64, I, P, P, P, P, I, F, I]
+            lib.oracle_rmsnorm_modulate_f64.restype = None
+            lib.oracle_rmsnorm_modulate_emulate_bf16.restype = None
             lib.oracle_allowed_pairs.argtypes = [I, I, I, I, P, P, P]
             lib.oracle_allowed_pairs.restype = ctypes.c_int64
             for fn in ("oracle_qk_norm_rope_f64", "oracle_qk_norm_rope_emulate_bf16",
@@ -172,3 +181,34 @@ def allowed_pairs(B, Sq, Sk, causal=False, kv_len=None, q_len=None, causal_b=Non
     q_len = None if q_len is None else np.ascontiguousarray(q_len, dtype=np.int32)
     causal_b = None if causal_b is None else np.ascontiguousarray(causal_b, dtype=np.uint8)
     return int(_load().oracle_allowed_pairs(B, Sq, Sk, int(bool(causal)), _p(kv_len), _p(q_len), _p(causal_b)))
+
+
+def _mod_args(x, w, scale, shift, idx):
+    T, C = x.shape
+    assert x.dtype == np.uint16 and C % 8 == 0
+    N = scale.shape[0]
+    assert scale.shape == (N, C) and shift.shape == (N, C) and scale.dtype == np.uint16 and shift.dtype == np.uint16
+    w = None if w is None else np.ascontiguousarray(w, dtype=np.float32)
+    idx = None if idx is None else np.ascontiguousarray(idx, dtype=np.int32)
+    assert idx is None or idx.shape == (T,)
+    return T, C, N, np.ascontiguousarray(x), w, np.ascontiguousarray(scale), np.ascontiguousarray(shift), idx
+
+
+def rmsnorm_modulate_f64(x, w, scale, shift, idx, eps, nthreads=0):
+    """x: bf16 bits [T, C]; w: [C] float32 or None; scale, shift: bf16 bits [N, C];
+    idx: int32 [T] or None (all rows use index 0).  Returns bf16 bits [T, C]:
+    the fp64 definition, each bf16 boundary a single rounding of the exact value."""
+    T, C, N, x, w, scale, shift, idx = _mod_args(x, w, scale, shift, idx)
+    y = np.empty((T, C), dtype=np.uint16)
+    _load().oracle_rmsnorm_modulate_f64(_p(x), _p(y), T, C, _p(w), _p(scale), _p(shift), _p(idx), N,
+                                        float(eps), nthreads)
+    return y
+
+
+def rmsnorm_modulate_emulate(x, w, scale, shift, idx, eps, nthreads=0):
+    """Same arguments; the float32 fixed-order emulation (bit-exact contract)."""
+    T, C, N, x, w, scale, shift, idx = _mod_args(x, w, scale, shift, idx)
+    y = np.empty((T, C), dtype=np.uint16)
+    _load().oracle_rmsnorm_modulate_emulate_bf16(_p(x), _p(y), T, C, _p(w), _p(scale), _p(shift), _p(idx), N,
+                                                 float(np.float32(eps)), nthreads)
+    return y

@@ -19,6 +19,9 @@
  *      GQA, cross-attention, causal, key-padding and boolean [Q, K] mask
  *      variants (FastVideo PR #1832, "Summary"; FastVideo PR #1799,
  *      "Implementation").
+ *   5. RMSNorm of a DiT hidden row followed by indexed AdaLN scale/shift
+ *      modulation, keeping the bf16 store/load boundaries of the unfused
+ *      norm-then-modulate path (TeleFuser PR #37 section 2.5).
  *
  * Precision: every step of the definition runs in double precision (fp64);
  * bf16 inputs widen exactly.  The one exception is
@@ -260,6 +263,121 @@ void oracle_qk_norm_rope_emulate_bf16(const uint16_t* x, uint16_t* out, int64_t 
                                       int rotary_dim, float eps, int nthreads) {
   nr32_ctx c = {x, out, S, H, D, w, cos_t, sin_t, rotary_dim, eps};
   parallel_for(rows, nthreads, nr32_rows, &c);
+}
+
+/* ------------------------------------------------------------------ */
+/* 5. RMSNorm -> indexed AdaLN scale/shift modulation                   */
+/*                                                                      */
+/* The unfused path it replaces, with a bf16 store after every step:    */
+/*   n = bf16(x * r * w)          r = 1/sqrt(mean_c(x_c^2) + eps)        */
+/*   a = bf16(1 + scale[idx[t]])  m = bf16(n * a)                        */
+/*   y = bf16(m + shift[idx[t]])                                         */
+/* w is optional (absent = 1).  Rows whose index is outside [0, N) are   */
+/* written as zeros.                                                     */
+/* ------------------------------------------------------------------ */
+typedef struct {
+  const uint16_t* x;
+  uint16_t* y;
+  int C, N;
+  const float* w;
+  const uint16_t* scale;
+  const uint16_t* shift;
+  const int32_t* idx;
+  double eps;
+  float epsf;
+} mod_ctx;
+
+/* Definition in fp64: every bf16 boundary rounds the exact value once. */
+static void mod64_rows(void* p, int64_t r0, int64_t r1) {
+  const mod_ctx* c = (const mod_ctx*)p;
+  int C = c->C;
+  for (int64_t t = r0; t < r1; ++t) {
+    const uint16_t* xr = c->x + t * C;
+    uint16_t* yr = c->y + t * C;
+    int32_t ix = c->idx ? c->idx[t] : 0;
+    if (ix < 0 || ix >= c->N) {
+      for (int ch = 0; ch < C; ++ch) yr[ch] = 0;
+      continue;
+    }
+    double ss = 0.0;
+    for (int ch = 0; ch < C; ++ch) {
+      double v = bf16_to_f64(xr[ch]);
+      ss += v * v;
+    }
+    double rinv = 1.0 / sqrt(ss / (double)C + c->eps);
+    const uint16_t* sc = c->scale + (int64_t)ix * C;
+    const uint16_t* sh = c->shift + (int64_t)ix * C;
+    for (int ch = 0; ch < C; ++ch) {
+      double n = round_f64_to_bf16(bf16_to_f64(xr[ch]) * rinv * (c->w ? (double)c->w[ch] : 1.0));
+      double a = round_f64_to_bf16(1.0 + bf16_to_f64(sc[ch]));
+      double m = round_f64_to_bf16(n * a);
+      yr[ch] = f64_to_bf16_bits(m + bf16_to_f64(sh[ch]));
+    }
+  }
+}
+
+void oracle_rmsnorm_modulate_f64(const uint16_t* x, uint16_t* y, int64_t T, int C, const float* w,
+                                 const uint16_t* scale, const uint16_t* shift, const int32_t* idx, int N,
+                                 double eps, int nthreads) {
+  mod_ctx c = {x, y, C, N, w, scale, shift, idx, eps, (float)eps};
+  parallel_for(T, nthreads, mod64_rows, &c);
+}
+
+/* The same step in float32 with a fixed operation order (the bit-exact    */
+/* contract for a CUDA implementation):                                    */
+/*   8-channel groups g = 0 .. C/8-1; group g belongs to lane g mod 32;    */
+/*   per lane acc = 0; acc = fmaf(x, x, acc) over its groups in increasing */
+/*   g, channels in order; butterfly over the 32 lanes: for off = 16 .. 1: */
+/*   p[l] = p[l] + p[l ^ off];  ms = sum / C;  r = 1 / sqrtf(ms + eps)     */
+/*   (each operation IEEE correctly rounded);  n = bf16((x * r) * w)       */
+/*   (n = bf16(x * r) without w);  a = bf16(1 + s);  m = bf16(n * a);       */
+/*   y = bf16(m + sh), every rounding to nearest even.                     */
+static void mod32_rows(void* p, int64_t r0, int64_t r1) {
+  const mod_ctx* c = (const mod_ctx*)p;
+  int C = c->C, G = C / 8;
+  float part[32];
+  for (int64_t t = r0; t < r1; ++t) {
+    const uint16_t* xr = c->x + t * C;
+    uint16_t* yr = c->y + t * C;
+    int32_t ix = c->idx ? c->idx[t] : 0;
+    if (ix < 0 || ix >= c->N) {
+      for (int ch = 0; ch < C; ++ch) yr[ch] = 0;
+      continue;
+    }
+    for (int l = 0; l < 32; ++l) {
+      float acc = 0.0f;
+      for (int g = l; g < G; g += 32)
+        for (int e = 0; e < 8; ++e) {
+          float xv = bf16_to_f32(xr[8 * g + e]);
+          acc = fmaf(xv, xv, acc);
+        }
+      part[l] = acc;
+    }
+    for (int off = 16; off >= 1; off /= 2) {
+      float nxt[32];
+      for (int l = 0; l < 32; ++l) nxt[l] = part[l] + part[l ^ off];
+      memcpy(part, nxt, sizeof(part));
+    }
+    float ms = part[0] / (float)C;
+    float rinv = 1.0f / sqrtf(ms + c->epsf);
+    const uint16_t* sc = c->scale + (int64_t)ix * C;
+    const uint16_t* sh = c->shift + (int64_t)ix * C;
+    for (int ch = 0; ch < C; ++ch) {
+      float v = bf16_to_f32(xr[ch]) * rinv;
+      if (c->w) v = v * c->w[ch];
+      float n = bf16_to_f32(f32_to_bf16_rne(v));
+      float a = bf16_to_f32(f32_to_bf16_rne(1.0f + bf16_to_f32(sc[ch])));
+      float m = bf16_to_f32(f32_to_bf16_rne(n * a));
+      yr[ch] = f32_to_bf16_rne(m + bf16_to_f32(sh[ch]));
+    }
+  }
+}
+
+void oracle_rmsnorm_modulate_emulate_bf16(const uint16_t* x, uint16_t* y, int64_t T, int C, const float* w,
+                                          const uint16_t* scale, const uint16_t* shift, const int32_t* idx,
+                                          int N, float eps, int nthreads) {
+  mod_ctx c = {x, y, C, N, w, scale, shift, idx, (double)eps, eps};
+  parallel_for(T, nthreads, mod32_rows, &c);
 }
 
 /* ------------------------------------------------------------------ */

@@ -33,3 +33,15 @@ def test_norm_rope_hand_example():
                                     np.array(case["sin"], np.float32).reshape(1, half),
                                     case["rotary_dim"], case["eps"], round_boundary=False)
         np.testing.assert_allclose(y[0, 0, 0], case["y"], rtol=1e-14, err_msg=case["name"])
+
+
+def test_rmsnorm_modulate_hand_example():
+    for case in G["rmsnorm_modulate"]:
+        C = len(case["x"])
+        x = _bits(case["x"])[None, :]
+        sc = np.full((1, C), _bits([case["scale"]])[0], np.uint16)
+        sh = np.full((1, C), _bits([case["shift"]])[0], np.uint16)
+        for fn in (oracle.rmsnorm_modulate_f64, oracle.rmsnorm_modulate_emulate):
+            y = fn(x.copy(), None, sc, sh, None, case["eps"])
+            got = (y.astype(np.uint32) << 16).view(np.float32)[0]
+            np.testing.assert_array_equal(got, np.array(case["y"], np.float32), err_msg=f"{case['name']} {fn.__name__}")
