@@ -280,6 +280,8 @@ def run_gpu(args):
     barrier()
     e2e_ms = e0.elapsed_time(e1)
 
+    mod = _time_rmsnorm_modulate(h3, gen, torch, stream, peaks) if args.modulate else None
+
     times = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
     if ws > 1:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
@@ -359,11 +361,46 @@ def run_gpu(args):
             "ms_per_launch": round(norm_ms, 4),
         },
     }
+    if mod is not None:
+        line["rmsnorm_modulate"] = mod
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def _time_rmsnorm_modulate(h3, gen, torch, stream, peaks, steps=20, warmup=3):
+    """The fused RMSNorm -> indexed AdaLN modulation kernel on its hidden-row
+    workload (x and y, 201 MB each, are larger than L2: no flush needed)."""
+    import numpy as np
+    mw = gen.MOD_WORKLOADS["dit_hidden_adaln"]
+    mi = gen.make_modulate_inputs(mw.T, mw.C, mw.frames, seed=0)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+    x, sc, sh = dev(mi.x), dev(mi.scale), dev(mi.shift)
+    y = torch.empty_like(x)
+    w, idx = torch.from_numpy(mi.w).cuda(), torch.from_numpy(mi.idx).cuda()
+    for _ in range(warmup):
+        h3.h3attn_rmsnorm_modulate(x, y, w, sc, sh, idx, mw.eps, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        h3.h3attn_rmsnorm_modulate(x, y, w, sc, sh, idx, mw.eps, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st = h3.h3attn_check_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after rmsnorm_modulate")
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = 2.0 * mw.T * mw.C * 2 + 2.0 * mw.frames * mw.C * 2 + mw.C * 4 + mw.T * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "rmsnorm_modulate_kernel<12>", "workload": f"{mw.name}: T={mw.T} C={mw.C} N={mw.frames}",
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": int(nbytes),
+            "ms_per_launch": round(ms, 4), "launches": steps + warmup}
 
 
 # The library's choice of attention kernel: one query tile per CTA (Q held in
@@ -485,6 +522,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--no-modulate", dest="modulate", action="store_false", default=True,
+                    help="skip the RMSNorm -> AdaLN modulation measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)

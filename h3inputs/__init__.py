@@ -35,6 +35,7 @@ STREAM_Q, STREAM_K, STREAM_V = 1, 2, 3
 STREAM_WQ, STREAM_WK = 4, 5
 STREAM_KVLEN, STREAM_BITS = 6, 7
 STREAM_TEXT_K, STREAM_TEXT_V = 8, 9
+STREAM_HIDDEN, STREAM_NORM_W, STREAM_SCALE, STREAM_SHIFT = 10, 11, 12, 13
 
 
 def _src_hash() -> str:
@@ -218,3 +219,42 @@ def make_inputs(wl: Workload, seed: int, nthreads: int = 0) -> Inputs:
     if wl.causal_pattern is not None:
         causal_b = np.array(wl.causal_pattern, dtype=np.uint8)
     return Inputs(wl, q, k, v, wq, wk, cos, sin, kv_len, causal_b)
+
+
+# RMSNorm -> indexed AdaLN modulation of DiT hidden rows (TeleFuser PR #37
+# section 2.5).  The pages give no shapes for it; the workload takes the
+# hidden rows of the long-video clip (T = 32760 tokens) at the hidden size
+# of its attention (C = 24 heads x 128 = 3072), one modulation row per latent
+# frame (21 frames of 1560 tokens; the index of a token is its frame).
+@dataclasses.dataclass(frozen=True)
+class ModWorkload:
+    name: str
+    T: int
+    C: int
+    frames: int
+    eps: float = 1e-6
+
+
+MOD_WORKLOADS = {
+    "dit_hidden_adaln": ModWorkload("dit_hidden_adaln", 32760, 3072, 21),
+}
+
+
+@dataclasses.dataclass
+class ModInputs:
+    x: np.ndarray      # bf16 bits [T, C]
+    w: np.ndarray      # float32 [C]
+    scale: np.ndarray  # bf16 bits [N, C]
+    shift: np.ndarray  # bf16 bits [N, C]
+    idx: np.ndarray    # int32 [T]
+
+
+def make_modulate_inputs(T, C, N, seed, nthreads: int = 0) -> ModInputs:
+    """Hidden rows N(0,1), weight U(0.5,1.5), modulation tables N(0, 0.3^2),
+    token t in table row t * N // T (contiguous runs, like frames)."""
+    x = normal_bshd(1, T, 1, C, seed, STREAM_HIDDEN, 1.0, 0.0, nthreads)[0, :, 0]
+    w = uniform_f32(C, seed, STREAM_NORM_W, 0.5, 1.5)
+    scale = normal_bshd(1, N, 1, C, seed, STREAM_SCALE, 0.3)[0, :, 0]
+    shift = normal_bshd(1, N, 1, C, seed, STREAM_SHIFT, 0.3)[0, :, 0]
+    idx = (np.arange(T, dtype=np.int64) * N // max(T, 1)).astype(np.int32)
+    return ModInputs(np.ascontiguousarray(x), w, np.ascontiguousarray(scale), np.ascontiguousarray(shift), idx)

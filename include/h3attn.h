@@ -155,6 +155,36 @@ h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void
                                int Sk, int Hq, int Hkv, int D, float scale,
                                const h3attn_mask_t* mask, int causal, h3attn_stream_t stream);
 
+/*
+ * Fused RMSNorm -> indexed AdaLN scale/shift modulation of DiT hidden rows
+ * (TeleFuser PR #37 "perf(minimax-h3): optimize Ulysses attention and DiT
+ * kernels", section 2.5: "RMSNorm -> indexed scale/shift modulation" in one
+ * kernel, keeping the bf16 store/load rounding boundaries of the unfused
+ * path).  For every row t of C channels, with s = scale[idx[t]] and
+ * h = shift[idx[t]]:
+ *   r = 1 / sqrt(mean_c(x_c^2) + eps)
+ *   n = bf16((x * r) * w)       (bf16(x * r) when w is NULL)
+ *   y = bf16(bf16(n * bf16(1 + s)) + h)
+ * The float32 operation order is fixed (8-channel groups dealt round-robin to
+ * 32 lanes, per-lane fused multiply-adds in channel order, a 32-lane
+ * butterfly, correctly rounded divide and square root, round-to-nearest-even
+ * stores), so results are reproducible bit for bit.
+ *
+ * x: [T, C] bf16 (device); y: [T, C] bf16 output (device), may be x itself.
+ * w: [C] float32 RMSNorm weight (device) or NULL.
+ * scale, shift: [N, C] bf16 modulation tables (device), row = index value.
+ * idx: [T] int32 (device): the table row of each token, or NULL for row 0.
+ *    A row whose index is outside [0, N) is written as zeros and
+ *    h3attn_check_device_status() then reports H3ATTN_ERR_INVALID_ARG.
+ * C a multiple of 8, 8 <= C <= 8192; N >= 1; eps >= 0 and finite; T == 0 is a
+ * no-op.  x, y, scale, shift, w 16-byte aligned, idx 4-byte aligned; y must not
+ * overlap scale, shift, w, idx or (unless equal) x.
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_DEVICE, LAUNCH.
+ */
+h3attn_status_t h3attn_rmsnorm_modulate(const void* x, void* y, const float* w, const void* scale,
+                                        const void* shift, const int32_t* idx, int T, int C, int N,
+                                        float eps, h3attn_stream_t stream);
+
 /* Static English description of a status code (never NULL). */
 const char* h3attn_status_string(h3attn_status_t status);
 

@@ -27,8 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_status_string",
-              "h3attn_check_device_status", "h3attn_version"):
+    for n in ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_rmsnorm_modulate",
+              "h3attn_status_string", "h3attn_check_device_status", "h3attn_version"):
         assert n in names
     assert set(names) == set(h3.EXPORTED)
 
@@ -116,3 +116,21 @@ def test_norm_rope_out_validation(lib):
     assert norm_out(lib, D=80) == h3.H3ATTN_ERR_UNSUPPORTED_HEAD_DIM
     assert norm_out(lib, B=0) == h3.H3ATTN_OK
     assert norm_out(lib, q=None, Hq=0, q_out=None, k=None, Hkv=0, k_out=None) == h3.H3ATTN_OK
+
+
+def modulate(lib, x=FAKE, y=FAKE * 100, w=FAKE * 200, scale=FAKE * 300, shift=FAKE * 400, idx=FAKE * 500, T=16,
+             C=256, N=4, eps=1e-6):
+    return lib.h3attn_rmsnorm_modulate(x, y, w, scale, shift, idx, T, C, N, eps, None)
+
+
+def test_rmsnorm_modulate_validation(lib):
+    assert modulate(lib, C=12) == h3.H3ATTN_ERR_INVALID_ARG        # not a multiple of 8
+    assert modulate(lib, C=8200) == h3.H3ATTN_ERR_INVALID_ARG      # above 8192
+    assert modulate(lib, N=0) == h3.H3ATTN_ERR_INVALID_ARG
+    assert modulate(lib, eps=-1.0) == h3.H3ATTN_ERR_INVALID_ARG
+    assert modulate(lib, scale=None) == h3.H3ATTN_ERR_INVALID_ARG
+    assert modulate(lib, x=FAKE + 8) == h3.H3ATTN_ERR_MISALIGNED
+    assert modulate(lib, idx=FAKE * 500 + 2) == h3.H3ATTN_ERR_MISALIGNED
+    assert modulate(lib, y=FAKE + 512) == h3.H3ATTN_ERR_INVALID_ARG      # partly over x
+    assert modulate(lib, y=FAKE * 300) == h3.H3ATTN_ERR_INVALID_ARG      # over the scale table
+    assert modulate(lib, T=0) == h3.H3ATTN_OK

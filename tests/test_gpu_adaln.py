@@ -1,0 +1,77 @@
+"""GPU parity of the fused RMSNorm -> indexed AdaLN scale/shift modulation
+kernel, called through the C ABI: bit-exact against the oracle's float32
+fixed-order emulation (the contract of TeleFuser PR #37 section 2.5:
+element-wise bit-exact with the unfused path), on the hidden-row workload and
+on edge cases (ragged group counts, the largest C, no weight, no index, in
+place, an index outside the table)."""
+import numpy as np
+import pytest
+
+import h3inputs as gen
+import oracle
+from helpers import from_dev, to_dev_f32, to_dev_i32
+
+
+def _dev2(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _run(h3, inp, with_w=True, with_idx=True, in_place=False, eps=1e-6):
+    import torch
+    x = _dev2(inp.x)
+    y = x if in_place else torch.full_like(x, float("nan"))
+    h3.h3attn_rmsnorm_modulate(x, y, to_dev_f32(inp.w) if with_w else None, _dev2(inp.scale), _dev2(inp.shift),
+                               to_dev_i32(inp.idx) if with_idx else None, eps)
+    torch.cuda.synchronize()
+    return from_dev(y)
+
+
+def _expect(inp, with_w=True, with_idx=True, eps=1e-6):
+    return oracle.rmsnorm_modulate_emulate(inp.x, inp.w if with_w else None, inp.scale, inp.shift,
+                                           inp.idx if with_idx else None, eps)
+
+
+def _assert_bits_equal(got, ref, what):
+    bad = np.flatnonzero(got.reshape(-1) != ref.reshape(-1))
+    assert bad.size == 0, f"{what}: {bad.size} of {got.size} elements differ, first at {bad[:5]}"
+
+
+@pytest.mark.gpu
+def test_bit_exact_on_hidden_row_workload(h3):
+    wl = gen.MOD_WORKLOADS["dit_hidden_adaln"]
+    inp = gen.make_modulate_inputs(wl.T, wl.C, wl.frames, seed=42)
+    got = _run(h3, inp, eps=wl.eps)
+    assert h3.h3attn_check_device_status() == 0
+    _assert_bits_equal(got, _expect(inp, eps=wl.eps), wl.name)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T,C,N", [(1, 8, 1), (7, 264, 3), (33, 1536, 5), (9, 8192, 2), (130, 5120, 4)])
+def test_bit_exact_edge_shapes(h3, T, C, N):
+    inp = gen.make_modulate_inputs(T, C, N, seed=T + C)
+    for with_w in (True, False):
+        got = _run(h3, inp, with_w=with_w)
+        assert h3.h3attn_check_device_status() == 0
+        _assert_bits_equal(got, _expect(inp, with_w=with_w), f"T={T} C={C} w={with_w}")
+
+
+@pytest.mark.gpu
+def test_no_index_and_in_place(h3):
+    inp = gen.make_modulate_inputs(50, 3072, 4, seed=5)
+    got = _run(h3, inp, with_idx=False)
+    _assert_bits_equal(got, _expect(inp, with_idx=False), "no index")
+    got = _run(h3, inp, in_place=True)
+    _assert_bits_equal(got, _expect(inp), "in place")
+    assert h3.h3attn_check_device_status() == 0
+
+
+@pytest.mark.gpu
+def test_index_outside_the_table_gives_zero_rows_and_an_error_status(h3):
+    inp = gen.make_modulate_inputs(12, 256, 3, seed=9)
+    inp.idx[[2, 7]] = [3, -1]
+    got = _run(h3, inp)
+    assert h3.h3attn_check_device_status() == h3.H3ATTN_ERR_INVALID_ARG
+    assert h3.h3attn_check_device_status() == 0  # the status word is cleared once read
+    _assert_bits_equal(got, _expect(inp), "bad index rows")
+    assert np.all(got[[2, 7]] == 0)

@@ -15,6 +15,10 @@ The entry points mirror the C ABI in ``include/h3attn.h``:
   separate outputs, leaving the raw q and k in place (SGLang PR #37903
   "[diffusion] model: support VDN-H3 ...", section "Modifications": the
   out-of-place variant, bit-equal to the in-place one, keeps the raw q/k).
+* ``h3attn_rmsnorm_modulate(x, y, w, scale, shift, idx, eps, stream)`` --
+  fused RMSNorm -> indexed AdaLN scale/shift modulation of DiT hidden rows
+  with the bf16 boundaries of the unfused path (TeleFuser PR #37, section
+  2.5).
 * ``h3attn_prefill(q, k, v, o, scale, mask, causal, stream)`` -- dense
   prefill attention on BSHD bf16 tensors with GQA, cross-attention, causal
   and boolean-mask variants (FastVideo PR #1799 "Add opt-in FlashInfer
@@ -40,8 +44,8 @@ H3ATTN_ERR_LAUNCH = 6
 H3ATTN_ERR_TIMEOUT = 7
 
 # Every symbol include/h3attn.h declares.
-EXPORTED = ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_status_string",
-            "h3attn_check_device_status", "h3attn_version")
+EXPORTED = ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_rmsnorm_modulate",
+            "h3attn_status_string", "h3attn_check_device_status", "h3attn_version")
 
 
 class H3AttnError(RuntimeError):
@@ -79,6 +83,8 @@ def load(path: str = LIB_PATH):
             lib.h3attn_qk_norm_rope.restype = I
             lib.h3attn_qk_norm_rope_out.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
             lib.h3attn_qk_norm_rope_out.restype = I
+            lib.h3attn_rmsnorm_modulate.argtypes = [P, P, P, P, P, P, I, I, I, F, P]
+            lib.h3attn_rmsnorm_modulate.restype = I
             lib.h3attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, F,
                                            ctypes.POINTER(h3attn_mask_t), I, P]
             lib.h3attn_prefill.restype = I
@@ -215,6 +221,31 @@ def h3attn_prefill(q, k, v, o, scale=None, mask: Mask | None = None, causal=Fals
                              int(bool(causal)), _stream_handle(stream))
     _raise_if(st, "h3attn_prefill")
     return o
+
+
+def h3attn_rmsnorm_modulate(x, y, w, scale, shift, idx=None, eps=1e-6, stream=None):
+    """y <- bf16(bf16(bf16(rmsnorm(x) * w) * bf16(1 + scale[idx])) + shift[idx]) row by row.
+
+    x, y: [T, C] bf16 CUDA tensors (y may be x); w: [C] float32 or None;
+    scale, shift: [N, C] bf16; idx: [T] int32 or None (table row 0 for all).
+    """
+    import torch
+    load()
+    for name, t in (("x", x), ("y", y), ("scale", scale), ("shift", shift)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+            raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must be a contiguous 2-D bf16 CUDA tensor")
+    T, C = x.shape
+    N = scale.shape[0]
+    if tuple(y.shape) != (T, C) or tuple(scale.shape) != (N, C) or tuple(shift.shape) != (N, C):
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "shape mismatch between x, y, scale and shift")
+    if w is not None and (w.dtype != torch.float32 or not w.is_cuda or w.numel() != C):
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"w must be a [{C}] float32 CUDA tensor")
+    if idx is not None and (idx.dtype != torch.int32 or not idx.is_cuda or idx.numel() != T):
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"idx must be a [{T}] int32 CUDA tensor")
+    st = _lib.h3attn_rmsnorm_modulate(_ptr(x), _ptr(y), _ptr(w), _ptr(scale), _ptr(shift), _ptr(idx), T, C, N,
+                                      float(eps), _stream_handle(stream))
+    _raise_if(st, "h3attn_rmsnorm_modulate")
+    return y
 
 
 def h3attn_check_device_status(stream=None) -> int:

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libh3attn.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "qk_norm_rope.cu", "attn_fwd.cu"]
+SOURCES = ["api.cu", "qk_norm_rope.cu", "attn_fwd.cu", "rmsnorm_modulate.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "attn_pipe.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

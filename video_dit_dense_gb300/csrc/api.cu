@@ -230,6 +230,40 @@ h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void
   return e == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_LAUNCH;
 }
 
+h3attn_status_t h3attn_rmsnorm_modulate(const void* x, void* y, const float* w, const void* scale,
+                                        const void* shift, const int32_t* idx, int T, int C, int N,
+                                        float eps, h3attn_stream_t stream) {
+  if (T < 0 || C <= 0 || C % 8 != 0 || C > h3::kModMaxChannels || N < 1) return H3ATTN_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !isfinite(eps)) return H3ATTN_ERR_INVALID_ARG;
+  if (T == 0) return H3ATTN_OK;
+  if (!x || !y || !scale || !shift) return H3ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(scale) || !aligned16(shift) || (w && !aligned16(w)) ||
+      (idx && (reinterpret_cast<uintptr_t>(idx) & 3u)))
+    return H3ATTN_ERR_MISALIGNED;
+  const int64_t ny = static_cast<int64_t>(T) * C * 2, nt = static_cast<int64_t>(N) * C * 2;
+  if (y != x && overlap(y, ny, x, ny)) return H3ATTN_ERR_INVALID_ARG;
+  if (overlap(y, ny, scale, nt) || overlap(y, ny, shift, nt) || (w && overlap(y, ny, w, static_cast<int64_t>(C) * 4)) ||
+      (idx && overlap(y, ny, idx, static_cast<int64_t>(T) * 4)))
+    return H3ATTN_ERR_INVALID_ARG;
+  h3attn_status_t st = check_device();
+  if (st != H3ATTN_OK) return st;
+  h3::ModArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.y = static_cast<uint16_t*>(y);
+  a.w = w;
+  a.scale = static_cast<const uint16_t*>(scale);
+  a.shift = static_cast<const uint16_t*>(shift);
+  a.idx = idx;
+  a.T = T;
+  a.C = C;
+  a.N = N;
+  a.eps = eps;
+  a.status = h3::status_word_ptr();
+  if (!a.status) return H3ATTN_ERR_LAUNCH;
+  cudaError_t e = h3::launch_rmsnorm_modulate(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_LAUNCH;
+}
+
 h3attn_status_t h3attn_check_device_status(h3attn_stream_t stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return H3ATTN_ERR_LAUNCH;
   int v = 0;

@@ -53,6 +53,23 @@ struct NormRopeArgs {
 };
 cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
 
+// ---- RMSNorm -> indexed AdaLN scale/shift modulation ----
+struct ModArgs {
+  const uint16_t* x;      // [T, C] bf16
+  uint16_t* y;            // [T, C] bf16 (may be x)
+  const float* w;         // [C] or nullptr
+  const uint16_t* scale;  // [N, C] bf16
+  const uint16_t* shift;  // [N, C] bf16
+  const int32_t* idx;     // [T] or nullptr (row 0 for every token)
+  int64_t T;
+  int C, N;
+  float eps;
+  int* status;            // device status word (out-of-range index)
+};
+// Largest C the kernel holds in registers (32 groups of 8 channels per lane).
+constexpr int kModMaxChannels = 8192;
+cudaError_t launch_rmsnorm_modulate(const ModArgs& a, cudaStream_t stream);
+
 // ---- dense prefill attention ----
 struct AttnArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D (D, H, S, B) bf16 maps, 64-element inner box, 128B swizzle
