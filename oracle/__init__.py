@@ -20,6 +20,10 @@ What it computes (all in double precision, from the definitions):
   shift[idx] with the bf16 store after every step of the unfused path
   (TeleFuser PR #37 section 2.5); fp64 definition and the float32
   fixed-order contract of the CUDA kernel.
+* ``attention_window_f64`` -- self-attention under the chunked window with
+  anchor frames of SGLang PR #37903 ("Modifications", hybrid_window_attn_h3):
+  anchor rows and keys dense, any other query attends the keys of the chunks
+  within the radius of its own (the anchor frames shift the chunk grid).
 * ``attention_f64`` -- softmax(Q K^T * scale) V per output row with GQA,
   cross-attention, causal, key-padding and packed boolean [Q, K] masks
   (FastVideo PR #1799 "Add opt-in FlashInfer attention backend for Wan",
@@ -87,6 +91,10 @@ def _load():
             lib.oracle_rmsnorm_modulate_emulate_bf16.restype = None
             lib.oracle_allowed_pairs.argtypes = [I, I, I, I, P, P, P]
             lib.oracle_allowed_pairs.restype = ctypes.c_int64
+            lib.oracle_attention_window_f64.argtypes = [P, P, P, I, I, I, I, I, D, I, I, I, I, P, P, P, I64, P, I]
+            lib.oracle_attention_window_f64.restype = None
+            lib.oracle_window_allowed_pairs.argtypes = [I, I, I, I, I, I]
+            lib.oracle_window_allowed_pairs.restype = ctypes.c_int64
             for fn in ("oracle_qk_norm_rope_f64", "oracle_qk_norm_rope_emulate_bf16",
                        "oracle_attention_f64", "oracle_round_f64_to_bf16"):
                 getattr(lib, fn).restype = None
@@ -212,3 +220,29 @@ def rmsnorm_modulate_emulate(x, w, scale, shift, idx, eps, nthreads=0):
     _load().oracle_rmsnorm_modulate_emulate_bf16(_p(x), _p(y), T, C, _p(w), _p(scale), _p(shift), _p(idx), N,
                                                  float(np.float32(eps)), nthreads)
     return y
+
+
+def attention_window_f64(q, k, v, scale, frame_tokens, anchor_frames, chunk_frames, radius, kv_len=None,
+                         q_len=None, row_ids=None, nthreads=0):
+    """Self-attention rows in fp64 under the chunked window (q, k, v as attention_f64, Sq == Sk)."""
+    B, S, Hq, D = q.shape
+    assert k.shape[:2] == (B, S) and v.shape == k.shape and Hq % k.shape[2] == 0
+    assert frame_tokens > 0 and chunk_frames > 0 and anchor_frames >= 0 and radius >= 0
+    kv_len = None if kv_len is None else np.ascontiguousarray(kv_len, dtype=np.int32)
+    q_len = None if q_len is None else np.ascontiguousarray(q_len, dtype=np.int32)
+    if row_ids is None:
+        out = np.empty((B, S, Hq, D), dtype=np.float64)
+        n, rid = B * S * Hq, None
+    else:
+        rid = np.ascontiguousarray(row_ids, dtype=np.int64)
+        n = rid.size
+        out = np.empty((n, D), dtype=np.float64)
+    _load().oracle_attention_window_f64(_p(q), _p(k), _p(v), B, S, Hq, k.shape[2], D, float(scale), frame_tokens,
+                                        anchor_frames, chunk_frames, radius, _p(kv_len), _p(q_len), _p(rid), n,
+                                        _p(out), nthreads)
+    return out
+
+
+def window_allowed_pairs(S, L, frame_tokens, anchor_frames, chunk_frames, radius) -> int:
+    """Allowed (query row, key) pairs of one sample under the window and key padding L."""
+    return int(_load().oracle_window_allowed_pairs(S, L, frame_tokens, anchor_frames, chunk_frames, radius))

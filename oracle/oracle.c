@@ -394,7 +394,23 @@ typedef struct {
   const uint32_t* bits;    /* [B, Sq, ceil(Sk/32)] or NULL */
   const int64_t* row_ids;  /* flat BSHD row ids ((b*Sq + i)*Hq + h), or NULL for all rows */
   double* out;             /* [nrows, D] */
+  /* chunked window (self-attention): 0 tokens per chunk = no window */
+  int64_t win_af;          /* anchor tokens: anchor_frames * frame_tokens */
+  int64_t win_ct;          /* tokens per chunk: chunk_frames * frame_tokens */
+  int64_t win_r;           /* radius in chunks */
 } att_ctx;
+
+/* Chunked window with anchor frames (SGLang PR #37903, "Modifications",
+   hybrid_window_attn_h3: chunk-5 / radius-1 window with anchor frames,
+   dense-query rows against all keys; "Accuracy Tests": the anchor frames
+   shift the chunk grid).  Rows and keys of the anchor frames are dense; any
+   other query in chunk c = (i - af) / ct attends the keys of chunks
+   c - r .. c + r. */
+static int window_allows(int64_t af, int64_t ct, int64_t r, int64_t i, int64_t j) {
+  if (ct <= 0 || i < af || j < af) return 1;
+  int64_t d = (i - af) / ct - (j - af) / ct;
+  return d <= r && d >= -r;
+}
 
 /* Whether query row i of sample b may attend key j. */
 static int allowed(const att_ctx* c, int b, int64_t i, int64_t j) {
@@ -407,6 +423,7 @@ static int allowed(const att_ctx* c, int b, int64_t i, int64_t j) {
     uint32_t word = c->bits[((int64_t)b * c->Sq + i) * W + (j >> 5)];
     if (!((word >> (j & 31)) & 1u)) return 0;
   }
+  if (!window_allows(c->win_af, c->win_ct, c->win_r, i, j)) return 0;
   return 1;
 }
 
@@ -467,9 +484,44 @@ void oracle_attention_f64(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           const int32_t* kv_len, const int32_t* q_len, const uint8_t* causal_b,
                           const uint32_t* bits, const int64_t* row_ids, int64_t nrows, double* out,
                           int nthreads) {
-  att_ctx c = {q, k, v, B, Sq, Sk, Hq, Hkv, D, scale, causal, kv_len, q_len, causal_b, bits, row_ids, out};
+  att_ctx c = {q, k, v, B, Sq, Sk, Hq, Hkv, D, scale, causal, kv_len, q_len, causal_b, bits, row_ids, out, 0, 0, 0};
   int64_t n = row_ids ? nrows : (int64_t)B * Sq * Hq;
   parallel_for(n, nthreads, att_rows, &c);
+}
+
+/* Self-attention under the chunked window (plus optional key padding and
+   zero tail): frame_tokens F, anchor_frames A, chunk_frames K, radius r. */
+void oracle_attention_window_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int S,
+                                 int Hq, int Hkv, int D, double scale, int frame_tokens, int anchor_frames,
+                                 int chunk_frames, int radius, const int32_t* kv_len, const int32_t* q_len,
+                                 const int64_t* row_ids, int64_t nrows, double* out, int nthreads) {
+  att_ctx c = {q, k, v, B, S, S, Hq, Hkv, D, scale, 0, kv_len, q_len, NULL, NULL, row_ids, out,
+               (int64_t)anchor_frames * frame_tokens, (int64_t)chunk_frames * frame_tokens, radius};
+  int64_t n = row_ids ? nrows : (int64_t)B * S * Hq;
+  parallel_for(n, nthreads, att_rows, &c);
+}
+
+/* Allowed (query row, key) pairs of one sample under the window and key
+   padding L: per row, the anchor keys plus the keys of the row's chunk
+   window, counted by intervals. */
+int64_t oracle_window_allowed_pairs(int S, int L, int frame_tokens, int anchor_frames, int chunk_frames,
+                                    int radius) {
+  int64_t af = (int64_t)anchor_frames * frame_tokens, ct = (int64_t)chunk_frames * frame_tokens;
+  int64_t total = 0;
+  if (L > S) L = S;
+  if (L < 0) L = 0;
+  for (int64_t i = 0; i < S; ++i) {
+    if (i < af) {
+      total += L;
+      continue;
+    }
+    int64_t ci = (i - af) / ct;
+    int64_t lo = af + (ci - radius) * ct, hi = af + (ci + radius + 1) * ct;
+    if (lo < af) lo = af;
+    if (hi > L) hi = L;
+    total += (af < L ? af : L) + (hi > lo ? hi - lo : 0);
+  }
+  return total;
 }
 
 /* Number of allowed (i, j) pairs, summed over samples and query rows (times
