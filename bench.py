@@ -281,6 +281,7 @@ def run_gpu(args):
     e2e_ms = e0.elapsed_time(e1)
 
     mod = _time_rmsnorm_modulate(h3, gen, torch, stream, peaks) if args.modulate else None
+    wnd = _time_window(h3, gen, torch, stream, peaks) if args.window else None
 
     times = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
     if ws > 1:
@@ -363,6 +364,8 @@ def run_gpu(args):
     }
     if mod is not None:
         line["rmsnorm_modulate"] = mod
+    if wnd is not None:
+        line["window_attention"] = wnd
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -401,6 +404,58 @@ def _time_rmsnorm_modulate(h3, gen, torch, stream, peaks, steps=20, warmup=3):
             "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": int(nbytes),
             "ms_per_launch": round(ms, 4), "launches": steps + warmup}
+
+
+def _window_pairs(S, L, frame_tokens, anchor_frames, chunk_frames, radius):
+    """Allowed (query row, key) pairs of one sample under the chunked window
+    and key padding L: anchor rows see every key; any other row sees the
+    anchor keys and the keys of the chunks within the radius of its own."""
+    import numpy as np
+    af, ct = anchor_frames * frame_tokens, chunk_frames * frame_tokens
+    L = max(0, min(L, S))
+    i = np.arange(af, S, dtype=np.int64)
+    ci = (i - af) // ct
+    lo = np.maximum(af + (ci - radius) * ct, af)
+    hi = np.minimum(af + (ci + radius + 1) * ct, L)
+    return int(min(af, S) * L + len(i) * min(af, L) + np.maximum(hi - lo, 0).sum())
+
+
+def _time_window(h3, gen, torch, stream, peaks, steps=5, warmup=3):
+    """The chunked-window prefill on the packed clip (q, k, v 641 MB each)."""
+    ww = gen.WINDOW_WORKLOADS["packed_clip_window"]
+
+    def dev(bits):
+        import numpy as np
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    q = dev(gen.normal_bshd(ww.B, ww.S, ww.H, ww.D, 0, gen.STREAM_Q))
+    k = dev(gen.normal_bshd(ww.B, ww.S, ww.H, ww.D, 0, gen.STREAM_K))
+    v = dev(gen.normal_bshd(ww.B, ww.S, ww.H, ww.D, 0, gen.STREAM_V))
+    o = torch.empty_like(q)
+    win = h3.Window(ww.frame_tokens, ww.anchor_frames, ww.chunk_frames, ww.radius)
+    for _ in range(warmup):
+        h3.h3attn_prefill_window(q, k, v, o, win, None, None, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        h3.h3attn_prefill_window(q, k, v, o, win, None, None, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st = h3.h3attn_check_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the window prefill")
+    ms = e0.elapsed_time(e1) / steps
+    pairs = ww.B * _window_pairs(ww.S, ww.S, ww.frame_tokens, ww.anchor_frames, ww.chunk_frames, ww.radius)
+    flops = 4.0 * ww.D * ww.H * pairs
+    tf = flops / (ms * 1e-3) / 1e12
+    dense = 4.0 * ww.B * ww.S * ww.S * ww.H * ww.D
+    return {"kernel": "attn_pipe_kernel<128,7> (window tile ranges)",
+            "workload": f"{ww.name}: B={ww.B} S={ww.S} H={ww.H} D={ww.D}; frames of {ww.frame_tokens} tokens, "
+                        f"{ww.anchor_frames} anchor frame, chunks of {ww.chunk_frames} frames, radius {ww.radius}",
+            "bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(tf / peaks["bf16_tflops"], 4), "flops_per_launch": flops,
+            "allowed_fraction": round(flops / dense, 4), "ms_per_launch": round(ms, 4),
+            "dense_equivalent_tflops": round(dense / (ms * 1e-3) / 1e12, 1), "launches": steps + warmup}
 
 
 # The library's choice of attention kernel: one query tile per CTA (Q held in
@@ -524,6 +579,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-modulate", dest="modulate", action="store_false", default=True,
                     help="skip the RMSNorm -> AdaLN modulation measurement")
+    ap.add_argument("--no-window", dest="window", action="store_false", default=True,
+                    help="skip the chunked-window attention measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)

@@ -258,3 +258,26 @@ def make_modulate_inputs(T, C, N, seed, nthreads: int = 0) -> ModInputs:
     shift = normal_bshd(1, N, 1, C, seed, STREAM_SHIFT, 0.3)[0, :, 0]
     idx = (np.arange(T, dtype=np.int64) * N // max(T, 1)).astype(np.int32)
     return ModInputs(np.ascontiguousarray(x), w, np.ascontiguousarray(scale), np.ascontiguousarray(shift), idx)
+
+
+# Chunked-window self-attention (SGLang PR #37903, hybrid_window_attn_h3:
+# chunk-5 / radius-1 window with anchor frames).  The page gives the clip
+# (~104k packed rows) but not its frame geometry; the workload reads the
+# packed clip's 104448 rows as 68 frames of 1536 tokens, one anchor frame,
+# chunks of 5 frames, radius 1, 24 heads of 128.
+@dataclasses.dataclass(frozen=True)
+class WindowWorkload:
+    name: str
+    B: int
+    S: int
+    H: int
+    D: int
+    frame_tokens: int
+    anchor_frames: int
+    chunk_frames: int
+    radius: int
+
+
+WINDOW_WORKLOADS = {
+    "packed_clip_window": WindowWorkload("packed_clip_window", 1, 104448, 24, 128, 1536, 1, 5, 1),
+}

@@ -185,6 +185,37 @@ h3attn_status_t h3attn_rmsnorm_modulate(const void* x, void* y, const float* w, 
                                         const void* shift, const int32_t* idx, int T, int C, int N,
                                         float eps, h3attn_stream_t stream);
 
+/*
+ * Chunked window of video self-attention with anchor frames (SGLang PR
+ * #37903 "[diffusion] model: support VDN-H3 ...", section "Modifications",
+ * hybrid_window_attn_h3: a chunk-5 / radius-1 window with anchor frames,
+ * dense-query rows against all keys; section "Accuracy Tests": the anchor
+ * frames shift the chunk grid).  Rows are frame-major video tokens; token t
+ * is in frame t / frame_tokens.  With af = anchor_frames * frame_tokens and
+ * ct = chunk_frames * frame_tokens:
+ *   allowed(i, j) = i < af  or  j < af  or  |(i - af) / ct - (j - af) / ct| <= radius
+ * (integer division), AND-ed with the key padding / zero tail of the mask.
+ */
+typedef struct {
+  int frame_tokens;   /* tokens per frame, >= 1 */
+  int anchor_frames;  /* leading frames whose queries and keys are dense, >= 0 */
+  int chunk_frames;   /* frames per chunk of the window grid, >= 1 */
+  int radius;         /* a query in chunk c attends chunks c - radius .. c + radius, >= 0 */
+} h3attn_window_t;
+
+/*
+ * Prefill self-attention (Sq = Sk = S) under the chunked window above; key
+ * tiles outside a query block's window are never loaded or computed.
+ * q, k, v, o, B, Hq, Hkv, scale as for h3attn_prefill(); D in {64, 128}.
+ * win: required.  mask: NULL or a descriptor whose kv_len / q_len apply as in
+ *    h3attn_prefill(); causal_b and bits are rejected (UNSUPPORTED_MASK).
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_HEAD_DIM (D = 256),
+ * UNSUPPORTED_DEVICE, UNSUPPORTED_MASK, LAUNCH.
+ */
+h3attn_status_t h3attn_prefill_window(const void* q, const void* k, const void* v, void* o, int B, int S,
+                                      int Hq, int Hkv, int D, float scale, const h3attn_window_t* win,
+                                      const h3attn_mask_t* mask, h3attn_stream_t stream);
+
 /* Static English description of a status code (never NULL). */
 const char* h3attn_status_string(h3attn_status_t status);
 

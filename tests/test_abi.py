@@ -27,8 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_rmsnorm_modulate",
-              "h3attn_status_string", "h3attn_check_device_status", "h3attn_version"):
+    for n in ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_prefill_window",
+              "h3attn_rmsnorm_modulate", "h3attn_status_string", "h3attn_check_device_status", "h3attn_version"):
         assert n in names
     assert set(names) == set(h3.EXPORTED)
 
@@ -134,3 +134,25 @@ def test_rmsnorm_modulate_validation(lib):
     assert modulate(lib, y=FAKE + 512) == h3.H3ATTN_ERR_INVALID_ARG      # partly over x
     assert modulate(lib, y=FAKE * 300) == h3.H3ATTN_ERR_INVALID_ARG      # over the scale table
     assert modulate(lib, T=0) == h3.H3ATTN_OK
+
+
+def window_call(lib, win=(16, 1, 5, 1), D=128, S=256, mask=None, q=FAKE, o=FAKE * 4):
+    w = ctypes.pointer(h3.h3attn_window_t(*win)) if win is not None else None
+    return lib.h3attn_prefill_window(q, FAKE * 2, FAKE * 3, o, 1, S, 4, 4, D, 0.088, w, mask, None)
+
+
+def test_prefill_window_validation(lib):
+    assert window_call(lib, win=None) == h3.H3ATTN_ERR_INVALID_ARG
+    assert window_call(lib, win=(0, 1, 5, 1)) == h3.H3ATTN_ERR_INVALID_ARG      # frame of no tokens
+    assert window_call(lib, win=(16, 1, 0, 1)) == h3.H3ATTN_ERR_INVALID_ARG     # chunk of no frames
+    assert window_call(lib, win=(16, -1, 5, 1)) == h3.H3ATTN_ERR_INVALID_ARG
+    assert window_call(lib, win=(16, 1, 5, -1)) == h3.H3ATTN_ERR_INVALID_ARG
+    assert window_call(lib, win=(1 << 20, 1, 1 << 12, 1)) == h3.H3ATTN_ERR_INVALID_ARG  # chunk tokens overflow
+    assert window_call(lib, D=256) == h3.H3ATTN_ERR_UNSUPPORTED_HEAD_DIM
+    m = h3.h3attn_mask_t(None, None, FAKE, None)
+    assert window_call(lib, mask=ctypes.pointer(m)) == h3.H3ATTN_ERR_UNSUPPORTED_MASK
+    m = h3.h3attn_mask_t(None, None, None, FAKE)
+    assert window_call(lib, mask=ctypes.pointer(m)) == h3.H3ATTN_ERR_UNSUPPORTED_MASK
+    assert window_call(lib, q=FAKE + 8) == h3.H3ATTN_ERR_MISALIGNED
+    assert window_call(lib, o=FAKE) == h3.H3ATTN_ERR_INVALID_ARG                 # o aliases q
+    assert window_call(lib, S=0) == h3.H3ATTN_OK

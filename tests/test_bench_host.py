@@ -36,3 +36,9 @@ def test_clock_summary_keeps_only_the_timed_window():
     rec = c.summarise(rows)
     assert rec["samples"] == 3 and rec["sm_mhz"] == 1750 and rec["sm_max_mhz"] == 2070
     assert rec["reasons"] == ["sw_power_cap"] and rec["window"] == "timed region"
+
+
+def test_window_pairs_match_oracle_count():
+    for S, L, geo in ((104448, 104448, (1536, 1, 5, 1)), (2000, 1500, (100, 1, 5, 1)), (777, 777, (7, 0, 3, 2)),
+                      (500, 500, (10, 60, 2, 1))):
+        assert bench._window_pairs(S, L, *geo) == oracle.window_allowed_pairs(S, L, *geo)

@@ -15,6 +15,9 @@ The entry points mirror the C ABI in ``include/h3attn.h``:
   separate outputs, leaving the raw q and k in place (SGLang PR #37903
   "[diffusion] model: support VDN-H3 ...", section "Modifications": the
   out-of-place variant, bit-equal to the in-place one, keeps the raw q/k).
+* ``h3attn_prefill_window(q, k, v, o, window, scale, mask, stream)`` -- the
+  chunked window with anchor frames of SGLang PR #37903 ("Modifications",
+  hybrid_window_attn_h3), key tiles outside a query block's window skipped.
 * ``h3attn_rmsnorm_modulate(x, y, w, scale, shift, idx, eps, stream)`` --
   fused RMSNorm -> indexed AdaLN scale/shift modulation of DiT hidden rows
   with the bf16 boundaries of the unfused path (TeleFuser PR #37, section
@@ -44,8 +47,8 @@ H3ATTN_ERR_LAUNCH = 6
 H3ATTN_ERR_TIMEOUT = 7
 
 # Every symbol include/h3attn.h declares.
-EXPORTED = ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_rmsnorm_modulate",
-            "h3attn_status_string", "h3attn_check_device_status", "h3attn_version")
+EXPORTED = ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_prefill_window",
+            "h3attn_rmsnorm_modulate", "h3attn_status_string", "h3attn_check_device_status", "h3attn_version")
 
 
 class H3AttnError(RuntimeError):
@@ -58,6 +61,11 @@ class H3AttnError(RuntimeError):
 class h3attn_mask_t(ctypes.Structure):
     _fields_ = [("kv_len", ctypes.c_void_p), ("q_len", ctypes.c_void_p),
                 ("causal_b", ctypes.c_void_p), ("bits", ctypes.c_void_p)]
+
+
+class h3attn_window_t(ctypes.Structure):
+    _fields_ = [("frame_tokens", ctypes.c_int), ("anchor_frames", ctypes.c_int),
+                ("chunk_frames", ctypes.c_int), ("radius", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -88,6 +96,9 @@ def load(path: str = LIB_PATH):
             lib.h3attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, F,
                                            ctypes.POINTER(h3attn_mask_t), I, P]
             lib.h3attn_prefill.restype = I
+            lib.h3attn_prefill_window.argtypes = [P, P, P, P, I, I, I, I, I, F, ctypes.POINTER(h3attn_window_t),
+                                                  ctypes.POINTER(h3attn_mask_t), P]
+            lib.h3attn_prefill_window.restype = I
             lib.h3attn_status_string.argtypes = [I]
             lib.h3attn_status_string.restype = ctypes.c_char_p
             lib.h3attn_check_device_status.argtypes = [P]
@@ -246,6 +257,40 @@ def h3attn_rmsnorm_modulate(x, y, w, scale, shift, idx=None, eps=1e-6, stream=No
                                       float(eps), _stream_handle(stream))
     _raise_if(st, "h3attn_rmsnorm_modulate")
     return y
+
+
+@dataclass
+class Window:
+    """Chunked window with anchor frames: see h3attn_window_t."""
+    frame_tokens: int
+    anchor_frames: int
+    chunk_frames: int
+    radius: int
+
+
+def h3attn_prefill_window(q, k, v, o, window: Window, scale=None, mask: Mask | None = None, stream=None):
+    """o <- windowed self-attention of q against k, v (BSHD bf16, Sq == Sk)."""
+    load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_bf16(name, t)
+    B, S, Hq, D = q.shape
+    if tuple(k.shape[:2]) != (B, S) or k.shape[3] != D or tuple(v.shape) != tuple(k.shape) or \
+            tuple(o.shape) != tuple(q.shape):
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "shape mismatch between q, k, v and o (self-attention)")
+    if scale is None:
+        scale = 1.0 / float(D) ** 0.5
+    mptr = None
+    if mask is not None:
+        if mask.bits is not None or mask.causal_b is not None:
+            raise H3AttnError(H3ATTN_ERR_UNSUPPORTED_MASK, "the window combines with kv_len / q_len only")
+        m = h3attn_mask_t(_ptr(mask.kv_len), _ptr(mask.q_len), None, None)
+        mptr = ctypes.pointer(m)
+    w = h3attn_window_t(int(window.frame_tokens), int(window.anchor_frames), int(window.chunk_frames),
+                        int(window.radius))
+    st = _lib.h3attn_prefill_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, S, Hq, k.shape[2], D, float(scale),
+                                    ctypes.pointer(w), mptr, _stream_handle(stream))
+    _raise_if(st, "h3attn_prefill_window")
+    return o
 
 
 def h3attn_check_device_status(stream=None) -> int:

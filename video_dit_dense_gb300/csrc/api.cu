@@ -177,14 +177,30 @@ h3attn_status_t h3attn_qk_norm_rope_out(const void* q, const void* k, void* q_ou
   return norm_rope(q, k, q_out, k_out, wq, wk, cos, sin, B, S, Hq, Hkv, D, rotary_dim, eps, stream);
 }
 
-h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Sq,
-                               int Sk, int Hq, int Hkv, int D, float scale,
-                               const h3attn_mask_t* mask, int causal, h3attn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of the dense and windowed prefill entry points (win == nullptr:
+// dense).
+h3attn_status_t prefill(const void* q, const void* k, const void* v, void* o, int B, int Sq, int Sk, int Hq,
+                        int Hkv, int D, float scale, const h3attn_mask_t* mask, int causal,
+                        const h3attn_window_t* win, h3attn_stream_t stream) {
   if (B < 0 || Sq < 0 || Sk < 1 || Hq < 1 || Hkv < 1) return H3ATTN_ERR_INVALID_ARG;
   if (!head_dim_ok(D)) return H3ATTN_ERR_UNSUPPORTED_HEAD_DIM;
   if (Hq % Hkv != 0) return H3ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || !isfinite(scale)) return H3ATTN_ERR_INVALID_ARG;
   if (B > 65535 || Hq > 65535) return H3ATTN_ERR_INVALID_ARG;
+  if (win) {
+    if (Sq != Sk || win->frame_tokens < 1 || win->chunk_frames < 1 || win->anchor_frames < 0 || win->radius < 0)
+      return H3ATTN_ERR_INVALID_ARG;
+    // token counts of the window grid must fit 32 bits
+    if (static_cast<int64_t>(win->frame_tokens) * win->chunk_frames > INT32_MAX ||
+        static_cast<int64_t>(win->frame_tokens) * win->anchor_frames > INT32_MAX)
+      return H3ATTN_ERR_INVALID_ARG;
+    if (D == 256) return H3ATTN_ERR_UNSUPPORTED_HEAD_DIM;
+    if (causal || (mask && (mask->causal_b || mask->bits))) return H3ATTN_ERR_UNSUPPORTED_MASK;
+  }
   if (B == 0 || Sq == 0) return H3ATTN_OK;
   if (!q || !k || !v || !o) return H3ATTN_ERR_INVALID_ARG;
   const bool any_causal = causal || (mask && mask->causal_b);
@@ -226,8 +242,37 @@ h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void
   // Kernel choice override (tests run every case on both kernels): "1" or "2".
   const char* kern = getenv("H3ATTN_ATTN_KERNEL");
   a.kernel = (kern && (kern[0] == '1' || kern[0] == '2')) ? kern[0] - '0' : 0;
+  a.win_ct = a.win_af = a.win_r = 0;
+  if (win) {
+    a.kernel = 1;  // the window's tile ranges live in the one-query-tile kernel
+    a.win_ct = win->frame_tokens * win->chunk_frames;
+    a.win_af = static_cast<int>(min(static_cast<int64_t>(win->frame_tokens) * win->anchor_frames,
+                                    static_cast<int64_t>(Sk)));
+    a.win_r = static_cast<int>(min(static_cast<int64_t>(win->radius), static_cast<int64_t>(Sk)));
+  }
   cudaError_t e = h3::launch_attention(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Sq,
+                               int Sk, int Hq, int Hkv, int D, float scale,
+                               const h3attn_mask_t* mask, int causal, h3attn_stream_t stream) {
+  return prefill(q, k, v, o, B, Sq, Sk, Hq, Hkv, D, scale, mask, causal, nullptr, stream);
+}
+
+h3attn_status_t h3attn_prefill_window(const void* q, const void* k, const void* v, void* o, int B, int S,
+                                      int Hq, int Hkv, int D, float scale, const h3attn_window_t* win,
+                                      const h3attn_mask_t* mask, h3attn_stream_t stream) {
+  if (!win) return H3ATTN_ERR_INVALID_ARG;
+  if (S == 0) {  // no tokens: nothing to do once the window itself is well formed
+    const bool ok = win->frame_tokens >= 1 && win->chunk_frames >= 1 && win->anchor_frames >= 0 && win->radius >= 0;
+    return ok ? H3ATTN_OK : H3ATTN_ERR_INVALID_ARG;
+  }
+  return prefill(q, k, v, o, B, S, S, Hq, Hkv, D, scale, mask, 0, win, stream);
 }
 
 h3attn_status_t h3attn_rmsnorm_modulate(const void* x, void* y, const float* w, const void* scale,

@@ -36,6 +36,8 @@
 // last allowed key of the CTA are never loaded.
 #include <cuda_bf16.h>
 
+#include <climits>
+
 #include "internal.h"
 #include "ptx.cuh"
 

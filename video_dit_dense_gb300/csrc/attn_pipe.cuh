@@ -91,7 +91,36 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   if (a.q_len) q_lim = min(q_lim, max(a.q_len[b], 0));
   int kv_end = kv_lim;
   if (causal) kv_end = min(kv_end, q0 + kBlockM);
-  const int n_tiles = (q0 >= q_lim || kv_end <= 0) ? 0 : (kv_end + kBlockN - 1) / kBlockN;
+  // Key tiles of this CTA: [0, n_lead) and [mid0, mid0 + n_tiles - n_lead).
+  // Dense: one range [0, ceil(kv_end / 128)).  Chunked window (self-attention,
+  // win_ct > 0): blocks holding an anchor row see every key; any other block
+  // sees the anchor keys [0, win_af) and the keys of the chunks within
+  // win_r of its rows' chunks.
+  int n_lead = 0, mid0 = 0, n_tiles = 0;
+  // keys every row of the block may attend: [0, full_a) and [full_lo, full_hi)
+  int full_a = kv_end, full_lo = 0, full_hi = 0;
+  if (q0 < q_lim && kv_end > 0) {
+    const int n_all = (kv_end + kBlockN - 1) / kBlockN;
+    n_tiles = n_all;
+    if (a.win_ct > 0) {
+      const int q_last = min(q0 + kBlockM, a.Sq) - 1;
+      if (q0 >= a.win_af) {
+        const int64_t af = a.win_af, ct = a.win_ct, r = a.win_r;
+        const int64_t c_lo = (q0 - af) / ct, c_hi = (q_last - af) / ct;
+        const int lo = static_cast<int>(af + max(c_lo - r, int64_t{0}) * ct);
+        const int hi = static_cast<int>(min(af + (c_hi + r + 1) * ct, static_cast<int64_t>(kv_end)));
+        n_lead = (min(a.win_af, kv_end) + kBlockN - 1) / kBlockN;
+        mid0 = max(lo / kBlockN, n_lead);
+        const int mid1 = hi > lo ? (hi + kBlockN - 1) / kBlockN : 0;
+        n_tiles = n_lead + max(mid1 - mid0, 0);
+        full_a = min(a.win_af, kv_end);
+        full_lo = static_cast<int>(min(af + max(c_hi - r, int64_t{0}) * ct, static_cast<int64_t>(INT_MAX)));
+        full_hi = static_cast<int>(min(af + (c_lo + r + 1) * ct, static_cast<int64_t>(kv_end)));
+      } else if (q_last >= a.win_af) {
+        full_a = 0;  // anchor rows and windowed rows share the block: mask every tile
+      }
+    }
+  }
   // Load order = consumption order: K_0, K_1, K_2, then K_{j+3} (if any) and
   // V_j for j = 0, 1, ...  Load index of V_j: the K loads up to
   // K_{min(j+3, n-1)} and the V loads before it; K_j (j >= 3) sits right
@@ -100,13 +129,17 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   auto ld_k = [](int j) { return j < 3 ? j : 2 * j - 3; };
   auto stage_of = [](int load) { return load % NSTAGE; };
   auto phase_of = [](int load) { return static_cast<uint32_t>((load / NSTAGE) & 1); };
-  // Iteration j visits key tile (j + rot) mod n_tiles.  The online softmax
+  // Iteration j visits entry (j + rot) mod n_tiles of the CTA's tile list.
+  // The online softmax
   // does not depend on the order of the key tiles; rotating the start by the
   // query block spreads the CTAs that run at the same time (neighbouring
   // query blocks of one head) over different K/V tiles instead of having all
   // of them read the same tile's lines at once.
   const int rot = n_tiles > 0 ? static_cast<int>(blockIdx.x) % n_tiles : 0;
-  auto tile_of = [rot, n_tiles](int j) { return j + rot < n_tiles ? j + rot : j + rot - n_tiles; };
+  auto tile_of = [rot, n_lead, mid0, n_tiles](int j) {
+    const int m = j + rot < n_tiles ? j + rot : j + rot - n_tiles;  // position in the CTA's tile list
+    return m < n_lead ? m : mid0 + (m - n_lead);
+  };
   // Tile j's barriers of parity j % 2 complete for the (j / 2)-th time.
   auto bpar = [](int j) { return static_cast<uint32_t>((j >> 1) & 1); };
 
@@ -225,6 +258,15 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
     const uint32_t tP = tmem + lane_off + C::kColP;
     const float sl = a.scale_log2;
     const int64_t bit_words = (a.Sk + 31) / 32;
+    // this row's window: anchor keys [0, win_a) and chunk keys [win_lo, win_hi)
+    int win_a = INT_MAX, win_lo = 0, win_hi = 0;
+    if (a.win_ct > 0 && row >= a.win_af) {
+      const int64_t af = a.win_af, ct = a.win_ct, r = a.win_r;
+      const int64_t ci = (row - af) / ct;
+      win_a = a.win_af;
+      win_lo = static_cast<int>(min(af + max(ci - r, int64_t{0}) * ct, static_cast<int64_t>(INT_MAX)));
+      win_hi = static_cast<int>(min(af + (ci + r + 1) * ct, static_cast<int64_t>(INT_MAX)));
+    }
     float m_ref = -INFINITY;  // running max in scaled (log2) units
     float l = 0.0f;
     bool ok = true;
@@ -261,7 +303,8 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + (j & 1) * 128;
       const int kbase = tile_of(j) * kBlockN;
-      const bool need_mask = (kbase + kBlockN > kv_lim) || (causal && kbase + kBlockN - 1 > q0) || a.bits;
+      const bool need_mask = (kbase + kBlockN > kv_lim) || (causal && kbase + kBlockN - 1 > q0) || a.bits ||
+                             (a.win_ct > 0 && kbase + kBlockN > full_a && (kbase < full_lo || kbase + kBlockN > full_hi));
       // First pass: exponentials against the running max as it stands.  That
       // is exactly the result of the rescale rule below whenever no score of
       // the tile exceeds the running max by more than kRescaleThreshold, and
@@ -286,6 +329,8 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
         if (need_mask) {
           int lim = kv_lim - kbase;
           if (causal) lim = min(lim, row + 1 - kbase);
+          // window: keys [0, w_a) and [w_lo, w_hi) relative to the tile
+          const int w_a = win_a - kbase, w_lo = win_lo - kbase, w_hi = win_hi - kbase;
           uint32_t wbits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
           if (a.bits && row < a.Sq) {
             const uint32_t* br = a.bits + (static_cast<int64_t>(b) * a.Sq + row) * bit_words;
@@ -297,7 +342,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
           }
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c) {
-            const bool allowed = (c < lim) && ((wbits[c >> 5] >> (c & 31)) & 1u);
+            const bool allowed = (c < lim) && ((wbits[c >> 5] >> (c & 31)) & 1u) && (c < w_a || (c >= w_lo && c < w_hi));
             s[c] = allowed ? s[c] : -INFINITY;
           }
         }

@@ -85,6 +85,9 @@ struct AttnArgs {
   uint64_t wait_limit_ns;
   int debug_skip_producer;  // fault injection for the bounded-wait test: 1 = never load K/V
   int kernel;               // 0 = choose by key length, 1 = one query tile per CTA, 2 = two
+  // chunked window (self-attention, one-query-tile kernel only): tokens per
+  // chunk (0 = dense), anchor tokens, radius in chunks
+  int win_ct, win_af, win_r;
 };
 // Key length from which the one-query-tile kernel is chosen (head_dim 64/128).
 constexpr int kOneTileMinKeys = 1024;
