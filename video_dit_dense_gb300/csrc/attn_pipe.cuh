@@ -51,7 +51,9 @@ struct PipeCfg {
   static_assert(NSTAGE >= 4, "K_{j+3}, V_j and the other thread's pair resident together");
 };
 
-template <int D, int NSTAGE>
+// WIN: chunked-window tile lists and masking (a.win_ct > 0); the dense
+// instantiation carries none of that code.
+template <int D, int NSTAGE, bool WIN>
 __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant__ AttnArgs a) {
   using C = PipeCfg<D, NSTAGE>;
   extern __shared__ uint8_t smem_raw[];
@@ -102,7 +104,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   if (q0 < q_lim && kv_end > 0) {
     const int n_all = (kv_end + kBlockN - 1) / kBlockN;
     n_tiles = n_all;
-    if (a.win_ct > 0) {
+    if constexpr (WIN) {
       const int q_last = min(q0 + kBlockM, a.Sq) - 1;
       if (q0 >= a.win_af) {
         const int64_t af = a.win_af, ct = a.win_ct, r = a.win_r;
@@ -138,7 +140,11 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   const int rot = n_tiles > 0 ? static_cast<int>(blockIdx.x) % n_tiles : 0;
   auto tile_of = [rot, n_lead, mid0, n_tiles](int j) {
     const int m = j + rot < n_tiles ? j + rot : j + rot - n_tiles;  // position in the CTA's tile list
-    return m < n_lead ? m : mid0 + (m - n_lead);
+    if constexpr (WIN) {
+      return m < n_lead ? m : mid0 + (m - n_lead);
+    } else {
+      return m;
+    }
   };
   // Tile j's barriers of parity j % 2 complete for the (j / 2)-th time.
   auto bpar = [](int j) { return static_cast<uint32_t>((j >> 1) & 1); };
@@ -260,7 +266,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
     const int64_t bit_words = (a.Sk + 31) / 32;
     // this row's window: anchor keys [0, win_a) and chunk keys [win_lo, win_hi)
     int win_a = INT_MAX, win_lo = 0, win_hi = 0;
-    if (a.win_ct > 0 && row >= a.win_af) {
+    if (WIN && row >= a.win_af) {
       const int64_t af = a.win_af, ct = a.win_ct, r = a.win_r;
       const int64_t ci = (row - af) / ct;
       win_a = a.win_af;
@@ -303,8 +309,8 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + (j & 1) * 128;
       const int kbase = tile_of(j) * kBlockN;
-      const bool need_mask = (kbase + kBlockN > kv_lim) || (causal && kbase + kBlockN - 1 > q0) || a.bits ||
-                             (a.win_ct > 0 && kbase + kBlockN > full_a && (kbase < full_lo || kbase + kBlockN > full_hi));
+      bool need_mask = (kbase + kBlockN > kv_lim) || (causal && kbase + kBlockN - 1 > q0) || a.bits;
+      if constexpr (WIN) need_mask = need_mask || (kbase + kBlockN > full_a && (kbase < full_lo || kbase + kBlockN > full_hi));
       // First pass: exponentials against the running max as it stands.  That
       // is exactly the result of the rescale rule below whenever no score of
       // the tile exceeds the running max by more than kRescaleThreshold, and
@@ -330,7 +336,12 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
           int lim = kv_lim - kbase;
           if (causal) lim = min(lim, row + 1 - kbase);
           // window: keys [0, w_a) and [w_lo, w_hi) relative to the tile
-          const int w_a = win_a - kbase, w_lo = win_lo - kbase, w_hi = win_hi - kbase;
+          int w_a = INT_MAX, w_lo = 0, w_hi = 0;
+          if constexpr (WIN) {
+            w_a = win_a - kbase;
+            w_lo = win_lo - kbase;
+            w_hi = win_hi - kbase;
+          }
           uint32_t wbits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
           if (a.bits && row < a.Sq) {
             const uint32_t* br = a.bits + (static_cast<int64_t>(b) * a.Sq + row) * bit_words;
@@ -342,7 +353,8 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
           }
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c) {
-            const bool allowed = (c < lim) && ((wbits[c >> 5] >> (c & 31)) & 1u) && (c < w_a || (c >= w_lo && c < w_hi));
+            bool allowed = (c < lim) && ((wbits[c >> 5] >> (c & 31)) & 1u);
+            if constexpr (WIN) allowed = allowed && (c < w_a || (c >= w_lo && c < w_hi));
             s[c] = allowed ? s[c] : -INFINITY;
           }
         }
@@ -469,7 +481,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
 template <int D, int NSTAGE>
 cudaError_t launch_pipe(const AttnArgs& a, cudaStream_t stream) {
   using C = PipeCfg<D, NSTAGE>;
-  auto kern = attn_pipe_kernel<D, NSTAGE>;
+  auto kern = a.win_ct > 0 ? attn_pipe_kernel<D, NSTAGE, true> : attn_pipe_kernel<D, NSTAGE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Sq + kBlockM - 1) / kBlockM, a.Hq, a.B);
