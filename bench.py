@@ -403,7 +403,8 @@ def _time_rmsnorm_modulate(h3, gen, torch, stream, peaks, steps=20, warmup=3):
     return {"kernel": "rmsnorm_modulate_kernel<12>", "workload": f"{mw.name}: T={mw.T} C={mw.C} N={mw.frames}",
             "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": int(nbytes),
-            "ms_per_launch": round(ms, 4), "launches": steps + warmup}
+            "ms_per_launch": round(ms, 4), "launches": steps + warmup,
+            "traffic": _profiled_traffic().get("mod")}
 
 
 def _window_pairs(S, L, frame_tokens, anchor_frames, chunk_frames, radius):
@@ -482,7 +483,7 @@ def _profiled_traffic():
         return out
     with open(p) as f:
         rec = json.load(f)
-    for key in ("attn", "norm"):
+    for key in ("attn", "norm", "mod"):
         r = rec.get(key)
         if not r:
             continue
