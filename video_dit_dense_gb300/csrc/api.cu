@@ -305,6 +305,7 @@ h3attn_status_t h3attn_rmsnorm_modulate(const void* x, void* y, const float* w, 
   a.eps = eps;
   a.status = h3::status_word_ptr();
   if (!a.status) return H3ATTN_ERR_LAUNCH;
+  a.wait_limit_ns = wait_limit_ns();
   cudaError_t e = h3::launch_rmsnorm_modulate(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_LAUNCH;
 }

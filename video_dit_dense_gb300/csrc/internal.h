@@ -64,9 +64,10 @@ struct ModArgs {
   int64_t T;
   int C, N;
   float eps;
-  int* status;            // device status word (out-of-range index)
+  int* status;            // device status word (out-of-range index, timeout)
+  uint64_t wait_limit_ns; // per-wait limit
 };
-// Largest C the kernel holds in registers (32 groups of 8 channels per lane).
+// Largest C: a 16 KiB row per shared-memory stage, at least two stages per CTA.
 constexpr int kModMaxChannels = 8192;
 cudaError_t launch_rmsnorm_modulate(const ModArgs& a, cudaStream_t stream);
 

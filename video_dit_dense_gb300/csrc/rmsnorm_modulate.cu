@@ -3,9 +3,9 @@
 // kernels", section 2.5: one kernel for "RMSNorm -> indexed scale/shift
 // modulation" that keeps the bf16 store/load rounding boundaries of the
 // unfused norm-then-modulate path, element-wise bit-exact with it).
-// Memory-bound: every row of x is read once and y written once (one warp per
-// row, the row held in registers between the two passes); the scale / shift
-// tables and the norm weight are small and stay in L1/L2.
+// Memory-bound: every row of x is read once (bulk-copied into a shared-memory
+// ring by a producer warp) and y written once; the scale / shift tables and
+// the norm weight are small and stay in L1/L2.
 //
 // For a row t of C channels, with s = scale[idx[t]], h = shift[idx[t]]:
 //   r = 1 / sqrt(mean_c(x_c^2) + eps)
@@ -25,7 +25,6 @@
 namespace h3 {
 namespace {
 
-constexpr int kModWarps = 8;  // rows per CTA, one warp per row
 
 __device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -49,103 +48,149 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// K = groups of 8 channels per lane (upper bound; groups past C/8 are skipped).
-template <int K>
-__global__ void __launch_bounds__(kModWarps * 32) rmsnorm_modulate_kernel(const __grid_constant__ ModArgs a) {
+// A persistent CTA streams its rows (blockIdx.x, blockIdx.x + gridDim.x, ...)
+// through a ring of NS one-row shared-memory stages: one producer warp
+// bulk-copies rows ahead as stages free up, and compute warp w takes rows
+// w, w + W, ... of the CTA's stream.  The ring keeps NS rows of HBM reads in
+// flight per CTA whatever the compute warps are doing.
+template <int W>
+__global__ void __launch_bounds__((W + 1) * 32) rmsnorm_modulate_kernel(const __grid_constant__ ModArgs a, int NS) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kModWarps + (threadIdx.x >> 5);
-  if (t >= a.T) return;
-  const int G = a.C >> 3;
-  const uint4* xr = reinterpret_cast<const uint4*>(a.x + t * a.C);
-  uint4* yr = reinterpret_cast<uint4*>(a.y + t * a.C);
-  const int32_t ix = a.idx ? a.idx[t] : 0;
-  if (ix < 0 || ix >= a.N) {
-    // no table row for this index: zeros, and the call reports an invalid argument
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const int g = lane + 32 * k;
-      if (g < G) yr[g] = make_uint4(0u, 0u, 0u, 0u);
+  const int C = a.C, G = C >> 3;
+  const uint32_t row_bytes = static_cast<uint32_t>(C) * 2;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + NS * row_bytes;
+  auto bar_full = [&](int st) { return bars + 8u * st; };
+  auto bar_empty = [&](int st) { return bars + 8u * (NS + st); };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + NS * row_bytes + 16 * NS);
+  WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(bar_full(st), 1);
+      mbar_init(bar_empty(st), 1);
     }
-    if (lane == 0) atomicExch(a.status, static_cast<int>(H3ATTN_ERR_INVALID_ARG));
-    return;
+    *abort_flag = 0u;
+    fence_barrier_init();
   }
-  uint4 xv[K];
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    const int g = lane + 32 * k;
-    xv[k] = g < G ? xr[g] : make_uint4(0u, 0u, 0u, 0u);
-  }
-  // sum of squares: this lane's groups in increasing g, channels in order
-  float acc = 0.0f;
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    if (lane + 32 * k < G) {
-      const uint32_t w4[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = __fmaf_rn(lo16(w4[e]), lo16(w4[e]), acc);
-        acc = __fmaf_rn(hi16(w4[e]), hi16(w4[e]), acc);
+  __syncthreads();
+  // rows of this CTA: a contiguous range t_i = r0 + i, i < n (neighbouring
+  // rows share their table row, which then stays in L1)
+  const int64_t per = (a.T + gridDim.x - 1) / gridDim.x;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * per;
+  const int64_t n = a.T > r0 ? min(per, a.T - r0) : 0;
+
+  if (warp == W) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      int64_t i = 0;
+      for (; i < n; ++i) {
+        const int st = static_cast<int>(i % NS);
+        if (!mbar_wait(bar_empty(st), static_cast<uint32_t>((i / NS) & 1) ^ 1u, ctl)) break;
+        mbar_arrive_expect_tx(bar_full(st), row_bytes);
+        bulk_load(sbase + st * row_bytes, a.x + (r0 + i) * C, row_bytes, bar_full(st));
+      }
+      // every issued copy has landed before the CTA retires
+      for (int64_t k = i > NS ? i - NS : 0; k < i; ++k) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar_full(static_cast<int>(k % NS)), static_cast<uint32_t>((k / NS) & 1)))
+          if (globaltimer_ns() - t0 > a.wait_limit_ns) break;
       }
     }
+    return;
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, off));
-  const float ms = __fdiv_rn(acc, static_cast<float>(a.C));
-  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
 
-  const uint4* sr = reinterpret_cast<const uint4*>(a.scale + static_cast<int64_t>(ix) * a.C);
-  const uint4* hr = reinterpret_cast<const uint4*>(a.shift + static_cast<int64_t>(ix) * a.C);
+  // ---------------- compute warps ----------------
   const uint32_t one2 = 0x3F803F80u;  // bf16x2 (1, 1)
+  for (int64_t i = warp; i < n; i += W) {
+    const int st = static_cast<int>(i % NS);
+    const bool ok = mbar_wait(bar_full(st), static_cast<uint32_t>((i / NS) & 1), ctl);
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    const int64_t t = r0 + i;
+    const uint4* xs = reinterpret_cast<const uint4*>(smem + st * row_bytes);
+    uint4* yr = reinterpret_cast<uint4*>(a.y + t * C);
+    const int32_t ix = a.idx ? a.idx[t] : 0;
+    if (ix < 0 || ix >= a.N) {
+      // no table row for this index: zeros, and the call reports an invalid argument
+      for (int g = lane; g < G; g += 32) yr[g] = make_uint4(0u, 0u, 0u, 0u);
+      if (lane == 0) atomicExch(a.status, static_cast<int>(H3ATTN_ERR_INVALID_ARG));
+    } else {
+      // sum of squares: this lane's groups in increasing g, channels in order
+      float acc = 0.0f;
+      for (int g = lane; g < G; g += 32) {
+        const uint4 v = xs[g];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int k = 0; k < K; ++k) {
-    const int g = lane + 32 * k;
-    if (g >= G) continue;
-    const uint4 sv = __ldg(sr + g), hv = __ldg(hr + g);
-    const uint32_t x4[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
-    const uint32_t s4[4] = {sv.x, sv.y, sv.z, sv.w};
-    const uint32_t h4[4] = {hv.x, hv.y, hv.z, hv.w};
-    float wv[8];
-    if (a.w) {
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.w + 8 * g));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.w + 8 * g + 4));
-      wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
-      wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
-    }
-    uint32_t out[4];
+        for (int e = 0; e < 4; ++e) {
+          acc = __fmaf_rn(lo16(w4[e]), lo16(w4[e]), acc);
+          acc = __fmaf_rn(hi16(w4[e]), hi16(w4[e]), acc);
+        }
+      }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float n0, n1;
-      fmul2(n0, n1, lo16(x4[e]), hi16(x4[e]), r, r);
-      if (a.w) fmul2(n0, n1, n0, n1, wv[2 * e], wv[2 * e + 1]);
-      const uint32_t nb = pack2(n0, n1);           // n = bf16(...)
-      const uint32_t ab = add_bf16x2(one2, s4[e]);  // a = bf16(1 + s)
-      const uint32_t mb = mul_bf16x2(nb, ab);       // m = bf16(n * a)
-      out[e] = add_bf16x2(mb, h4[e]);               // y = bf16(m + h)
+      for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, off));
+      const float ms = __fdiv_rn(acc, static_cast<float>(C));
+      const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+      const uint4* sr = reinterpret_cast<const uint4*>(a.scale + static_cast<int64_t>(ix) * C);
+      const uint4* hr = reinterpret_cast<const uint4*>(a.shift + static_cast<int64_t>(ix) * C);
+#pragma unroll 2
+      for (int g = lane; g < G; g += 32) {
+        const uint4 xv = xs[g], sv = __ldg(sr + g), hv = __ldg(hr + g);
+        const uint32_t x4[4] = {xv.x, xv.y, xv.z, xv.w};
+        const uint32_t s4[4] = {sv.x, sv.y, sv.z, sv.w};
+        const uint32_t h4[4] = {hv.x, hv.y, hv.z, hv.w};
+        float wv[8];
+        if (a.w) {
+          const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.w + 8 * g));
+          const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.w + 8 * g + 4));
+          wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+          wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+        }
+        uint32_t out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float n0, n1;
+          fmul2(n0, n1, lo16(x4[e]), hi16(x4[e]), r, r);
+          if (a.w) fmul2(n0, n1, n0, n1, wv[2 * e], wv[2 * e + 1]);
+          const uint32_t nb = pack2(n0, n1);           // n = bf16(...)
+          const uint32_t ab = add_bf16x2(one2, s4[e]);  // a = bf16(1 + s)
+          const uint32_t mb = mul_bf16x2(nb, ab);       // m = bf16(n * a)
+          out[e] = add_bf16x2(mb, h4[e]);               // y = bf16(m + h)
+        }
+        yr[g] = make_uint4(out[0], out[1], out[2], out[3]);
+      }
     }
-    yr[g] = make_uint4(out[0], out[1], out[2], out[3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty(st));  // the stage may be refilled
   }
-}
-
-template <int K>
-cudaError_t launch_k(const ModArgs& a, cudaStream_t stream) {
-  const int64_t blocks = (a.T + kModWarps - 1) / kModWarps;
-  rmsnorm_modulate_kernel<K><<<static_cast<unsigned>(blocks), kModWarps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_rmsnorm_modulate(const ModArgs& a, cudaStream_t stream) {
-  const int per_lane = (a.C / 8 + 31) / 32;  // groups of 8 channels per lane
-  if (per_lane <= 1) return launch_k<1>(a, stream);
-  if (per_lane <= 2) return launch_k<2>(a, stream);
-  if (per_lane <= 4) return launch_k<4>(a, stream);
-  if (per_lane <= 8) return launch_k<8>(a, stream);
-  if (per_lane <= 12) return launch_k<12>(a, stream);
-  if (per_lane <= 16) return launch_k<16>(a, stream);
-  if (per_lane <= 24) return launch_k<24>(a, stream);
-  if (per_lane <= 32) return launch_k<32>(a, stream);
-  return cudaErrorInvalidValue;
+  constexpr int W = 8;
+  const uint32_t row_bytes = static_cast<uint32_t>(a.C) * 2;
+  // about 96 KB of rows per CTA (two CTAs per SM), at least two stages
+  int NS = static_cast<int>((96u * 1024u) / row_bytes);
+  NS = NS < 2 ? 2 : (NS > 32 ? 32 : NS);
+  const size_t smem = static_cast<size_t>(NS) * row_bytes + 16 * NS + 16;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_set[dev]) {
+    // largest request: two 16 KiB rows (C = 8192) or 32 stages of 3 KiB, both under 128 KiB
+    e = cudaFuncSetAttribute(rmsnorm_modulate_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  int64_t blocks = static_cast<int64_t>(sms) * 2;
+  if (blocks > a.T) blocks = a.T;
+  rmsnorm_modulate_kernel<W><<<static_cast<unsigned>(blocks), (W + 1) * 32, smem, stream>>>(a, NS);
+  return cudaGetLastError();
 }
 
 }  // namespace h3
