@@ -196,8 +196,12 @@ void oracle_qk_norm_rope_f64(const uint16_t* x, double* y, int64_t rows, int S, 
 /* ------------------------------------------------------------------ */
 /* The same step in float32 with a fixed operation order (the bit-exact  */
 /* contract for a CUDA implementation):                                  */
-/*   lanes L = D/8, lane l owns channels [8l, 8l+8);                    */
-/*   per lane acc = 0; acc = fmaf(x, x, acc) over its 8 channels in order;*/
+/*   8-channel groups g = 0 .. D/8-1; h8 = rotary_dim/16 groups per      */
+/*   rotated half; L = D/16 lanes, each holding two groups: first group   */
+/*   g0 = l (l < h8) or L + l (l >= h8), second group g1 = l + h8, so a   */
+/*   lane l < h8 holds the rotation pair (l, l + h8);                     */
+/*   per lane acc = 0; acc = fmaf(x, x, acc) over the 8 channels of g0 in */
+/*   order, then those of g1;                                             */
 /*   butterfly over lanes: for off = L/2 .. 1: p[l] = p[l] + p[l ^ off];   */
 /*   ms = sum * (1/D) (exact power-of-two scaling);                       */
 /*   r = 1 / sqrtf(ms + eps), each operation IEEE correctly rounded;      */
@@ -218,7 +222,7 @@ typedef struct {
 
 static void nr32_rows(void* p, int64_t r0, int64_t r1) {
   const nr32_ctx* c = (const nr32_ctx*)p;
-  int D = c->D, half = c->rotary_dim / 2, L = D / 8;
+  int D = c->D, half = c->rotary_dim / 2, L = D / 16, h8 = c->rotary_dim / 16;
   float part[32];
   float nh[256];
   float y[256];
@@ -226,9 +230,15 @@ static void nr32_rows(void* p, int64_t r0, int64_t r1) {
     const uint16_t* xr = c->x + r * D;
     int64_t pos = (r / c->H) % c->S;
     for (int l = 0; l < L; ++l) {
+      int g0 = l < h8 ? l : L + l;
+      int g1 = l + h8;
       float acc = 0.0f;
       for (int e = 0; e < 8; ++e) {
-        float xv = bf16_to_f32(xr[8 * l + e]);
+        float xv = bf16_to_f32(xr[8 * g0 + e]);
+        acc = fmaf(xv, xv, acc);
+      }
+      for (int e = 0; e < 8; ++e) {
+        float xv = bf16_to_f32(xr[8 * g1 + e]);
         acc = fmaf(xv, xv, acc);
       }
       part[l] = acc;

@@ -13,15 +13,19 @@
 // q rows ([B*S*Hq, D]) and k rows ([B*S*Hkv, D]) are contiguous, so the work
 // is a list of 16 KiB chunks of whole rows.  A persistent grid walks the
 // chunk list; in each CTA one producer warp streams chunks into a ring of
-// shared-memory stages with 1-D bulk copies (completion on an mbarrier), and
-// eight compute warps read rows from shared memory, compute, and store the
-// results straight to global memory.  D/8 consecutive lanes own a row, each
-// holding 8 channels (one 16-byte access), so a warp covers 256/D... rows
-// per access and every access of a warp is 512 contiguous bytes.
+// shared-memory stages with 1-D bulk copies (completion on an mbarrier),
+// together with the RoPE table rows of the chunk's tokens, and eight compute
+// warps read rows from shared memory, compute, and store the results
+// straight to global memory.  D/16 lanes own a row, each holding two groups
+// of 8 channels (two 16-byte accesses): lane l < rotary_dim/16 holds a whole
+// rotation pair (channels 8l.. and 8l + rotary_dim/2..), so the rotation
+// needs no data from other lanes.
 //
 // Arithmetic (float32, fixed order -- reproducible bit for bit):
-//   lane partial: acc = fma(x, x, acc) over its 8 channels in order, from 0;
-//   butterfly over the row's lanes (xor offsets D/16 .. 1): acc = acc + partner;
+//   lane partial: acc = fma(x, x, acc) over its first group's 8 channels in
+//   order, then its second group's, from 0 (first group l or D/16 + l,
+//   second l + rotary_dim/16);
+//   butterfly over the row's lanes (xor offsets D/32 .. 1): acc = acc + partner;
 //   ms = acc * (1/D); r = 1 / sqrt(ms + eps), correctly rounded;
 //   n = bf16((x * r) * w); rotation with y_i = fma(a, c, -(b*s)),
 //   y_{i+h} = fma(b, c, a*s); store bf16(y) (round to nearest even).
@@ -40,11 +44,11 @@ constexpr int kStages = 3;     // row stages
 constexpr int kTabSlots = 6;   // RoPE table slots, released later than the rows
 constexpr int kNormThreads = (kComputeWarps + 1) * 32;  // + one producer warp
 constexpr int kChunkBytes = 16384;
-constexpr int kUnroll = 4;  // rows per lane slot per chunk; also rows sharing one sqrt/div pass
+constexpr int kUnroll = 2;  // rows per lane slot per chunk; also rows sharing one sqrt/div pass
 
 template <int D>
 struct NormCfg {
-  static constexpr int LPR = D / 8;                         // lanes per row
+  static constexpr int LPR = D / 16;                        // lanes per row (16 channels each)
   static constexpr int RPW = 32 / LPR;                      // rows per warp per access
   static constexpr int kRows = kChunkBytes / (D * 2);       // rows per chunk
   static_assert(kRows == kComputeWarps * RPW * kUnroll, "chunk = compute warps x rows per warp");
@@ -165,15 +169,18 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
   }
 
   // ---------------- compute warps ----------------
+  // A row's LPR = D/16 lanes each hold two 8-channel groups: first g0 = lr
+  // (lr < h8) or LPR + lr, second g1 = lr + h8, h8 = rotary_dim/16.  Lane
+  // lr < h8 thus holds a whole rotation pair (channel i and i + half); the
+  // others hold pass-through channels.  (Reading g0 then g1 is also free of
+  // shared-memory bank conflicts for D = 128.)
   const uint32_t lr = lane % LPR;  // lane within its row
   const uint32_t slot = lane / LPR;
   const uint32_t row_lane0 = lane - lr;
-  const uint32_t hl = static_cast<uint32_t>(half >> 3);  // lanes per rotated half
-  const bool rotating = lr < 2 * hl;
-  // Rotation partner: lanes [0, hl) pair with [hl, 2hl) of the same row.
-  const uint32_t partner = lr < hl ? lane + hl : (rotating ? lane - hl : lane);
-  const uint32_t ti = rotating ? (lr < hl ? lr : lr - hl) * 8 : 0;  // table column of this lane's channel 0
-  const uint32_t neg = lr < hl ? 0x80000000u : 0u;  // y_i takes -(b*s), y_{i+h} takes +(a*s)
+  const uint32_t h8 = static_cast<uint32_t>(half >> 3);
+  const bool rotating = lr < h8;
+  const uint32_t g0 = rotating ? lr : LPR + lr, g1 = lr + h8;
+  const uint32_t ti = lr * 8;  // table column of a rotating lane's channel 0
 
   uint32_t it = 0;
   for (uint32_t c = blockIdx.x; c < n_chunks; c += gridDim.x, ++it) {
@@ -191,25 +198,27 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
     chunk_tokens(is_q, row0, nrows, tok0, ntok);
     const bool staged = half > 0 && ntok <= static_cast<uint32_t>(C::kTabTokens) && ntok <= a.div_s.d;
 
-    uint4 xv[U];
+    uint4 xa[U], xb[U];
     uint32_t lrow[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       lrow[u] = (warp * U + u) * RPW + slot;
-      xv[u] = lrow[u] < nrows ? *reinterpret_cast<const uint4*>(stage + lrow[u] * (D * 2) + lr * 16)
-                              : make_uint4(0u, 0u, 0u, 0u);
+      const uint8_t* rp = stage + lrow[u] * (D * 2);
+      const bool live = lrow[u] < nrows;
+      xa[u] = live ? *reinterpret_cast<const uint4*>(rp + g0 * 16) : make_uint4(0u, 0u, 0u, 0u);
+      xb[u] = live ? *reinterpret_cast<const uint4*>(rp + g1 * 16) : make_uint4(0u, 0u, 0u, 0u);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty(st));  // the stage may be refilled
 
-    // Sum of squares: lane partial in channel order, then the butterfly.
+    // Sum of squares: g0's channels then g1's in order, then the butterfly.
     float acc[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint32_t w[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+      const uint32_t w[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w, xb[u].x, xb[u].y, xb[u].z, xb[u].w};
       float t = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 8; ++e) {
         const float x0 = bf16lo(w[e]), x1 = bf16hi(w[e]);
         t = __fmaf_rn(x0, x0, t);
         t = __fmaf_rn(x1, x1, t);
@@ -232,30 +241,30 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
 #pragma unroll
     for (int u = 0; u < U; ++u) rinv[u] = __shfl_sync(0xFFFFFFFFu, r_mine, row_lane0 + u);
 
-    const float* wp = (is_q ? a.wq : a.wk) + lr * 8;
-    const float4 w0 = __ldg(reinterpret_cast<const float4*>(wp));
-    const float4 w1 = __ldg(reinterpret_cast<const float4*>(wp + 4));
-    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const float* wp = is_q ? a.wq : a.wk;
+    const float4 wa0 = __ldg(reinterpret_cast<const float4*>(wp + g0 * 8));
+    const float4 wa1 = __ldg(reinterpret_cast<const float4*>(wp + g0 * 8 + 4));
+    const float4 wb0 = __ldg(reinterpret_cast<const float4*>(wp + g1 * 8));
+    const float4 wb1 = __ldg(reinterpret_cast<const float4*>(wp + g1 * 8 + 4));
+    const float wv[16] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w,
+                          wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
     const FastDiv& dh = is_q ? a.div_hq : a.div_hkv;
     uint16_t* gbase = is_q ? a.q_out : a.k_out;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+      if (lrow[u] >= nrows) continue;
+      const uint32_t xw[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w, xb[u].x, xb[u].y, xb[u].z, xb[u].w};
       // boundary values n^ = bf16((x * r) * w), kept as bf16 pairs
-      uint32_t nb[4];
+      uint32_t nb[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 8; ++e) {
         float t0, t1, n0, n1;
         fmul2(t0, t1, bf16lo(xw[e]), bf16hi(xw[e]), rinv[u], rinv[u]);
         fmul2(n0, n1, t0, t1, wv[2 * e], wv[2 * e + 1]);
         nb[e] = pack_bf16(n0, n1);
       }
-      uint32_t pb[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) pb[e] = __shfl_sync(0xFFFFFFFFu, nb[e], partner);
-      if (lrow[u] >= nrows) continue;
       const uint32_t r = row0 + lrow[u];
-      uint32_t ob[4] = {nb[0], nb[1], nb[2], nb[3]};
+      uint32_t ob[8] = {nb[0], nb[1], nb[2], nb[3], nb[4], nb[5], nb[6], nb[7]};
       if (rotating) {
         const uint32_t tok = fdiv(r, dh);
         float4 c0, c1, s0, s1;
@@ -276,20 +285,25 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
           s1 = __ldg(reinterpret_cast<const float4*>(stb + 4));
         }
         const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        // sine with this lane's sign folded in: (-s) * b == -(b * s) exactly
-        const float sv[8] = {__uint_as_float(__float_as_uint(s0.x) ^ neg), __uint_as_float(__float_as_uint(s0.y) ^ neg),
-                             __uint_as_float(__float_as_uint(s0.z) ^ neg), __uint_as_float(__float_as_uint(s0.w) ^ neg),
-                             __uint_as_float(__float_as_uint(s1.x) ^ neg), __uint_as_float(__float_as_uint(s1.y) ^ neg),
-                             __uint_as_float(__float_as_uint(s1.z) ^ neg), __uint_as_float(__float_as_uint(s1.w) ^ neg)};
+        const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        // pair (a, b) = (n_i, n_{i+half}):  y_i = fma(a, c, -(b*s)) with
+        // -(b*s) = b*(-s) exactly;  y_{i+half} = fma(b, c, a*s)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          float t0, t1, y0, y1;
-          fmul2(t0, t1, bf16lo(pb[e]), bf16hi(pb[e]), sv[2 * e], sv[2 * e + 1]);
-          ffma2(y0, y1, bf16lo(nb[e]), bf16hi(nb[e]), cv[2 * e], cv[2 * e + 1], t0, t1);
+          const float a0 = bf16lo(nb[e]), a1 = bf16hi(nb[e]);
+          const float b0 = bf16lo(nb[4 + e]), b1 = bf16hi(nb[4 + e]);
+          float t0, t1, u0, u1, y0, y1, z0, z1;
+          fmul2(t0, t1, b0, b1, -sv[2 * e], -sv[2 * e + 1]);
+          ffma2(y0, y1, a0, a1, cv[2 * e], cv[2 * e + 1], t0, t1);
+          fmul2(u0, u1, a0, a1, sv[2 * e], sv[2 * e + 1]);
+          ffma2(z0, z1, b0, b1, cv[2 * e], cv[2 * e + 1], u0, u1);
           ob[e] = pack_bf16(y0, y1);
+          ob[4 + e] = pack_bf16(z0, z1);
         }
       }
-      *reinterpret_cast<uint4*>(gbase + static_cast<size_t>(r) * D + lr * 8) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+      uint16_t* orow = gbase + static_cast<size_t>(r) * D;
+      *reinterpret_cast<uint4*>(orow + g0 * 8) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+      *reinterpret_cast<uint4*>(orow + g1 * 8) = make_uint4(ob[4], ob[5], ob[6], ob[7]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_tab_empty(ts));  // this warp is done with the table slot
