@@ -461,12 +461,15 @@ def _time_window(h3, gen, torch, stream, peaks, steps=5, warmup=3):
 
 # The library's choice of attention kernel: one query tile per CTA (Q held in
 # tensor memory) from 1024 keys on, for head dims 64 and 128; two query tiles
-# per CTA otherwise.  H3ATTN_ATTN_KERNEL=1/2 forces one or the other.
+# per CTA otherwise.  H3ATTN_ATTN_KERNEL=1/2 forces one or the other; 3 the
+# persistent one-CTA-per-SM kernel (head dims 64 and 128).
 ONE_TILE_MIN_KEYS = 1024
 
 
 def _attn_kernel_name(wl):
     sel = os.environ.get("H3ATTN_ATTN_KERNEL", "")
+    if sel == "3" and wl.D in (64, 128):
+        return {64: "attn_persist_kernel<64,12>", 128: "attn_persist_kernel<128,7>"}[wl.D]
     one_tile = wl.D in (64, 128) and (sel == "1" or (sel != "2" and wl.Sk >= ONE_TILE_MIN_KEYS))
     if one_tile:
         return {64: "attn_pipe_kernel<64,12>", 128: "attn_pipe_kernel<128,7>"}[wl.D]

@@ -74,6 +74,9 @@ def test_prefill_validation(lib):
     assert prefill(lib, mask=ctypes.pointer(m)) == h3.H3ATTN_ERR_MISALIGNED
     assert prefill(lib, q=None) == h3.H3ATTN_ERR_INVALID_ARG
     assert prefill(lib, o=FAKE) == h3.H3ATTN_ERR_INVALID_ARG  # o aliases q
+    assert prefill(lib, B=65536) == h3.H3ATTN_ERR_INVALID_ARG
+    # 2^31 work units (128-row query blocks x heads x batch) do not fit 32 bits
+    assert prefill(lib, B=4096, Sq=2**23, Sk=2**23, Hq=64, Hkv=64) == h3.H3ATTN_ERR_INVALID_ARG
     assert prefill(lib, B=0) == h3.H3ATTN_OK  # empty batch: no-op, nothing launched
     assert prefill(lib, Sq=0) == h3.H3ATTN_OK
 

@@ -40,10 +40,11 @@ def full_case(h3, B, Sq, Sk, Hq, Hkv, D, seed=0, causal=False, kv_len=None, q_le
 
 
 # ---------------------------------------------------------------- small / edge cases
-# Every edge case runs on both attention kernels: "1" = one query tile per CTA
-# (Q in tensor memory), "2" = two query tiles per CTA.  Without the override
-# the library picks by key length.
-@pytest.fixture(params=["1", "2"], ids=["one_tile", "two_tiles"])
+# Every edge case runs on every attention kernel: "1" = one query tile per CTA
+# (Q in tensor memory), "2" = two query tiles per CTA, "3" = the persistent
+# kernel (one CTA per SM over all units; head_dim 256 falls back to "2").
+# Without the override the library picks by key length.
+@pytest.fixture(params=["1", "2", "3"], ids=["one_tile", "two_tiles", "persistent"])
 def kernel(request, monkeypatch):
     monkeypatch.setenv("H3ATTN_ATTN_KERNEL", request.param)
     return request.param

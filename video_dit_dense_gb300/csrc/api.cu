@@ -191,6 +191,8 @@ h3attn_status_t prefill(const void* q, const void* k, const void* v, void* o, in
   if (Hq % Hkv != 0) return H3ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || !isfinite(scale)) return H3ATTN_ERR_INVALID_ARG;
   if (B > 65535 || Hq > 65535) return H3ATTN_ERR_INVALID_ARG;
+  // work units (128-row query blocks x heads x batch items) are counted in 32 bits
+  if ((static_cast<int64_t>(Sq) + 127) / 128 * Hq * B > INT32_MAX) return H3ATTN_ERR_INVALID_ARG;
   if (win) {
     if (Sq != Sk || win->frame_tokens < 1 || win->chunk_frames < 1 || win->anchor_frames < 0 || win->radius < 0)
       return H3ATTN_ERR_INVALID_ARG;
@@ -239,9 +241,9 @@ h3attn_status_t prefill(const void* q, const void* k, const void* v, void* o, in
   a.wait_limit_ns = wait_limit_ns();
   const char* inj = getenv("H3ATTN_FAULT_INJECT_STALL_PRODUCER");
   a.debug_skip_producer = (inj && inj[0] == '1') ? 1 : 0;
-  // Kernel choice override (tests run every case on both kernels): "1" or "2".
+  // Kernel choice override (tests run every case on every kernel): "1", "2" or "3".
   const char* kern = getenv("H3ATTN_ATTN_KERNEL");
-  a.kernel = (kern && (kern[0] == '1' || kern[0] == '2')) ? kern[0] - '0' : 0;
+  a.kernel = (kern && kern[0] >= '1' && kern[0] <= '3') ? kern[0] - '0' : 0;
   a.win_ct = a.win_af = a.win_r = 0;
   if (win) {
     a.kernel = 1;  // the window's tile ranges live in the one-query-tile kernel

@@ -452,6 +452,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
 }
 
 #include "attn_pipe.cuh"
+#include "attn_persist.cuh"
 
 template <int D, int NQ, int NSTAGE>
 cudaError_t launch_cfg(const AttnArgs& a, cudaStream_t stream) {
@@ -504,7 +505,12 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   // memory and two MMA-issuing threads (faster from about a thousand keys
   // on), or two query tiles per CTA sharing each K/V tile (faster on short
   // key ranges, where its shorter prologue matters).  a.kernel: 0 = by key
-  // length, 1 = one query tile, 2 = two query tiles.
+  // length, 1 = one query tile, 2 = two query tiles, 3 = the persistent
+  // kernel (one CTA per SM over all units; head_dim 64/128, not windowed).
+  if (a.kernel == 3 && a.win_ct == 0) {
+    if (a.D == 64) return launch_persist<64, 12>(a, stream);
+    if (a.D == 128) return launch_persist<128, 7>(a, stream);
+  }
   const bool one_tile = a.kernel == 1 || (a.kernel == 0 && a.Sk >= kOneTileMinKeys);
   switch (a.D) {
     case 64: return one_tile ? launch_pipe<64, 12>(a, stream) : launch_cfg<64, 2, 8>(a, stream);
