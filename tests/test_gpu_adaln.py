@@ -56,6 +56,20 @@ def test_bit_exact_edge_shapes(h3, T, C, N):
         _assert_bits_equal(got, _expect(inp, with_w=with_w), f"T={T} C={C} w={with_w}")
 
 
+# Every ring shape the launcher picks, with many rows per CTA so that each
+# compute warp goes round its CTA's ring several times (C 1536: 16 warps, 37
+# stages, 2 CTAs per SM; 4096 / 5120: 16 warps, 1 CTA; 8192: 8 warps, 14
+# stages, 1 CTA); every stage is refilled at least twice.  A ring with fewer
+# stages than compute warps would hand a warp a stale row here.
+@pytest.mark.gpu
+@pytest.mark.parametrize("T,C,N", [(24000, 1536, 4), (9000, 4096, 3), (7000, 5120, 3), (4500, 8192, 2)])
+def test_bit_exact_rows_lap_the_ring(h3, T, C, N):
+    inp = gen.make_modulate_inputs(T, C, N, seed=T ^ C)
+    got = _run(h3, inp)
+    assert h3.h3attn_check_device_status() == 0
+    _assert_bits_equal(got, _expect(inp), f"T={T} C={C}")
+
+
 @pytest.mark.gpu
 def test_no_index_and_in_place(h3):
     inp = gen.make_modulate_inputs(50, 3072, 4, seed=5)

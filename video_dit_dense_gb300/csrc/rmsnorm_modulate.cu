@@ -48,13 +48,21 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// A persistent CTA streams its rows (blockIdx.x, blockIdx.x + gridDim.x, ...)
-// through a ring of NS one-row shared-memory stages: one producer warp
-// bulk-copies rows ahead as stages free up, and compute warp w takes rows
-// w, w + W, ... of the CTA's stream.  The ring keeps NS rows of HBM reads in
-// flight per CTA whatever the compute warps are doing.
+// A persistent CTA streams a contiguous range of rows through a ring of NS
+// one-row shared-memory stages: one producer warp bulk-copies rows ahead as
+// stages free up, and compute warp w takes rows w, w + W, ... of the CTA's
+// range.  The ring keeps up to NS - W rows of HBM reads in flight per CTA
+// beyond the rows the compute warps hold.
+//
+// Ring invariant NS >= W (the launcher guarantees it).  When warp w waits for
+// row i (fill i / NS of stage i % NS), the stage's previous fill holds row
+// i - NS <= i - W; rows land in order and warp w has already consumed row
+// i - W, so that fill has landed and the phase parity names fill i / NS
+// unambiguously.  With NS < W a warp could find fill i / NS - 2 complete
+// instead and take a stale row.
 template <int W>
-__global__ void __launch_bounds__((W + 1) * 32) rmsnorm_modulate_kernel(const __grid_constant__ ModArgs a, int NS) {
+__global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
+    rmsnorm_modulate_kernel(const __grid_constant__ ModArgs a, int NS) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -165,32 +173,52 @@ __global__ void __launch_bounds__((W + 1) * 32) rmsnorm_modulate_kernel(const __
   }
 }
 
-}  // namespace
-
-cudaError_t launch_rmsnorm_modulate(const ModArgs& a, cudaStream_t stream) {
-  constexpr int W = 8;
-  const uint32_t row_bytes = static_cast<uint32_t>(a.C) * 2;
-  // about 96 KB of rows per CTA (two CTAs per SM), at least two stages
-  int NS = static_cast<int>((96u * 1024u) / row_bytes);
-  NS = NS < 2 ? 2 : (NS > 32 ? 32 : NS);
-  const size_t smem = static_cast<size_t>(NS) * row_bytes + 16 * NS + 16;
+template <int W>
+cudaError_t launch_with(const ModArgs& a, int ctas_per_sm, int NS, size_t smem, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !attr_set[dev]) {
-    // largest request: two 16 KiB rows (C = 8192) or 32 stages of 3 KiB, both under 128 KiB
-    e = cudaFuncSetAttribute(rmsnorm_modulate_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(rmsnorm_modulate_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  int64_t blocks = static_cast<int64_t>(sms) * 2;
+  int64_t blocks = static_cast<int64_t>(sms) * ctas_per_sm;
   if (blocks > a.T) blocks = a.T;
   rmsnorm_modulate_kernel<W><<<static_cast<unsigned>(blocks), (W + 1) * 32, smem, stream>>>(a, NS);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// Shape: as many compute warps per SM as the rings allow (the kernel is
+// latency-bound per warp: 16 compute warps per SM reached 4.44 TB/s, 32
+// reached 5.3 TB/s on T 32760 x C 3072), each ring holding at least W + 2
+// rows (the invariant NS >= W plus two rows of read-ahead), then the deepest
+// ring that fits beside the other CTAs of the SM.
+cudaError_t launch_rmsnorm_modulate(const ModArgs& a, cudaStream_t stream) {
+  constexpr int64_t kSmemPerSm = 233472;  // 228 KiB, of which 1 KiB per CTA is reserved
+  constexpr int64_t kMaxNS = 48;
+  const int64_t stage = static_cast<int64_t>(a.C) * 2 + 16;  // one row + its two barriers
+  struct Shape {
+    int W, ctas;
+  };
+  const Shape shapes[] = {{16, 2}, {8, 4}, {8, 3}, {16, 1}, {8, 2}, {8, 1}};
+  for (const Shape& sh : shapes) {
+    const int64_t per_cta = kSmemPerSm / sh.ctas - 1024 - 16;  // ring + abort word
+    int64_t NS = per_cta / stage;
+    if (NS < sh.W + 2) continue;
+    if (NS > kMaxNS) NS = kMaxNS;
+    const size_t smem = static_cast<size_t>(NS * stage + 16);
+    if (sh.W == 16) return launch_with<16>(a, sh.ctas, static_cast<int>(NS), smem, stream);
+    return launch_with<8>(a, sh.ctas, static_cast<int>(NS), smem, stream);
+  }
+  return cudaErrorInvalidValue;  // a row larger than the shared memory of an SM
 }
 
 }  // namespace h3
