@@ -400,7 +400,9 @@ def _time_rmsnorm_modulate(h3, gen, torch, stream, peaks, steps=20, warmup=3):
     ms = e0.elapsed_time(e1) / steps
     nbytes = 2.0 * mw.T * mw.C * 2 + 2.0 * mw.frames * mw.C * 2 + mw.C * 4 + mw.T * 4
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"kernel": "rmsnorm_modulate_kernel<8>", "workload": f"{mw.name}: T={mw.T} C={mw.C} N={mw.frames}",
+    # the launcher's shape: 16 compute warps per CTA while an 18-row ring fits one SM, else 8
+    w_mod = 16 if 18 * (2 * mw.C + 16) <= 233472 - 1040 else 8
+    return {"kernel": f"rmsnorm_modulate_kernel<{w_mod}>", "workload": f"{mw.name}: T={mw.T} C={mw.C} N={mw.frames}",
             "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": int(nbytes),
             "ms_per_launch": round(ms, 4), "launches": steps + warmup,
