@@ -60,7 +60,10 @@ typedef enum {
  *   causal_eff(b)    = causal argument != 0 or (causal_b != NULL and causal_b[b] != 0)
  *
  * kv_len[b] may be any int32: values <= 0 mask every key, values >= Sk mask
- * none.  A query row with no allowed key produces an all-zero output row.
+ * none.  K and V rows j >= kv_len[b] are padding and may hold anything
+ * (NaN, Inf): they never reach the output.  Keys masked only by causal or
+ * bits must hold finite K and V (their probability is zero, and 0 * NaN is
+ * NaN).  A query row with no allowed key produces an all-zero output row.
  * q_len[b]: rows i >= q_len[b] of sample b are written as zeros (the
  * fixed-valid zero-tail mode of TeleFuser PR #37 "perf(minimax-h3): optimize
  * Ulysses attention and DiT kernels", sections 2.3 and 2.4).

@@ -87,6 +87,29 @@ def test_bit_mask_and_q_len_and_degenerate(h3, kernel):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_poisoned_key_padding_is_never_attended(h3, kernel, D):
+    """Keys past kv_len hold NaN and Inf in K and V (as uninitialised padding
+    may): they must not reach the output.  kv_len falls inside a key tile, so
+    the tile that straddles it is loaded with its poisoned rows; the oracle
+    skips masked keys outright."""
+    B, S, Hq, Hkv = 2, 1300, 2, 1
+    kv_len = np.array([1000, 777], np.int32)
+    q = gen.normal_bshd(B, S, Hq, D, 21, gen.STREAM_Q)
+    k = gen.normal_bshd(B, S, Hkv, D, 21, gen.STREAM_K)
+    v = gen.normal_bshd(B, S, Hkv, D, 21, gen.STREAM_V)
+    for b in range(B):
+        for x in (k, v):
+            x[b, kv_len[b]:, :, 0::2] = 0x7FC0  # NaN
+            x[b, kv_len[b]:, :, 1::2] = 0x7F80  # +Inf
+    scale = 1.0 / np.sqrt(D)
+    got = gpu_attention(h3, q, k, v, scale, kv_len=kv_len)
+    ref = oracle.attention_f64(q, k, v, scale, False, kv_len, None, None)
+    assert np.all(np.isfinite(ref))
+    check_close(got, ref, f"poisoned padding D={D}")
+
+
+@pytest.mark.gpu
 def test_peaky_scores_exercise_rescaling(h3, kernel):
     """Large-magnitude inputs: maxima grow across key tiles, forcing O rescales."""
     full_case(h3, 1, 256, 1024, 2, 2, 128, seed=8, std=4.0, what="peaky")

@@ -57,7 +57,7 @@ struct Cfg {
   static constexpr int kChunkBytes = kBlockM * 128;       // 16 KiB: one swizzle column of a tile
   static constexpr int kSmemQ = NQ * kTileBytes;
   static constexpr int kSmemKV = NSTAGE * kTileBytes;
-  static constexpr int kNumBars = 1 + 2 * NSTAGE + 3 * NQ + 1;
+  static constexpr int kNumBars = 1 + 2 * NSTAGE + 3 * NQ + 2;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kSmemQ + kSmemKV + kNumBars * 8 + 16;
   // NQ softmax warpgroups + one control warpgroup (producer, MMA issuer, two idle warps)
   static constexpr int kThreads = NQ * 128 + 128;
@@ -103,6 +103,79 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
 
 __device__ int g_status_word = 0;
 
+// Shared-memory count: each producer thread adds with release, the waiter
+// reads with acquire (CTA scope).
+__device__ __forceinline__ void add_release_cta(uint32_t addr, uint32_t v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Wait until the count at addr reaches target; bounded like mbar_wait.
+__device__ __forceinline__ bool count_wait(uint32_t addr, uint32_t target, const WaitCtl& ctl) {
+  if (ld_acquire_cta(addr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (ld_acquire_cta(addr) >= target) return true;
+    if (*ctl.abort_flag) return false;
+    if (globaltimer_ns() - t0 > ctl.limit_ns) {
+      *ctl.abort_flag = 1u;
+      atomicExch(ctl.status, ctl.timeout_code);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void st_release_cta(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// count_wait for a warp with nothing else to do: sleeps between polls so that
+// it takes no issue slots from the warps that share its SM sub-partition.
+__device__ __forceinline__ bool count_wait_sleep(uint32_t addr, uint32_t target, const WaitCtl& ctl) {
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_cta(addr) < target) {
+    if (*ctl.abort_flag) return false;
+    if (globaltimer_ns() - t0 > ctl.limit_ns) {
+      *ctl.abort_flag = 1u;
+      atomicExch(ctl.status, ctl.timeout_code);
+      return false;
+    }
+    __nanosleep(256);
+  }
+  return true;
+}
+
+// Keys past kv_len may hold anything (uninitialised padding, NaN, Inf).  Their
+// scores are masked by selection, but in O += P V a zero probability times a
+// NaN or Inf value is still NaN, so in the key tile that straddles kv_len the
+// V rows r0 = kv_len mod 128 .. 127 are zeroed in shared memory before that
+// tile's O += P V is issued.  128-byte swizzle: row r of 64-channel chunk c is
+// the 128 bytes at c * 16 KiB + r * 128, its 16-byte units permuted among
+// themselves, so whole rows are contiguous: the calling thread `lane` of
+// `stride` writes 16-byte units lane, lane + stride, ... of that range
+// (neighbouring lanes on neighbouring units, no bank conflicts).  The proxy fence orders these generic writes before the
+// tensor core's reads, which follow a barrier the caller arrives on.
+// The zeroing warp learns that the V tile has landed in two steps: the
+// producer raises a flag in shared memory when it issues that load (the
+// stage's previous fill has then landed and been consumed), and only then
+// does the warp wait for the stage's phase, which from there on is
+// unambiguous; waiting on the phase alone from the kernel's start could pass
+// on a fill two rounds older (same parity).
+template <int D>
+__device__ __forceinline__ void zero_padding_rows(uint32_t tile, int r0, int lane, int stride) {
+  const int units = (kBlockN - r0) * 8;  // 16-byte units of rows r0 .. 127 in one chunk
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint32_t first = tile + c * 16384 + r0 * 128;
+    for (int k = lane; k < units; k += stride)
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(first + k * 16), "r"(0u) : "memory");
+  }
+  fence_proxy_async_smem();
+}
+
 #ifdef H3ATTN_TRACE
 // Optional pipeline trace (compile with -DH3ATTN_TRACE): clock64 stamps of
 // the first CTA's producer, MMA issuer and softmax threads, per key tile.
@@ -142,9 +215,11 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
   auto bar_p_ready = [&](int q) { return bars + 8u * (1 + 2 * NSTAGE + NQ + q); };
   auto bar_pv_done = [&](int q) { return bars + 8u * (1 + 2 * NSTAGE + 2 * NQ + q); };
   const uint32_t bar_drain = bars + 8u * (1 + 2 * NSTAGE + 3 * NQ);
+  const uint32_t bar_v_clean = bars + 8u * (2 + 2 * NSTAGE + 3 * NQ);  // padding rows of V zeroed
   uint8_t* gmisc = gbase + C::kSmemQ + C::kSmemKV + C::kNumBars * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gmisc + 4);
+  const uint32_t pad_issued = smem_u32(gmisc + 8);  // 1 once V of the tile straddling kv_len is requested
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -164,6 +239,11 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
   int kv_end = kv_lim;
   if (causal) kv_end = min(kv_end, q0 + NQ * kBlockM);
   int n_tiles = (q0 >= q_lim || kv_end <= 0) ? 0 : (kv_end + kBlockN - 1) / kBlockN;
+  // The key tile that straddles kv_len (keys from kv_len on are padding, read
+  // into the tile but never attended), or -1: none is loaded, or kv_len is Sk
+  // or a tile edge.  Its V rows past kv_len are zeroed before O += P V.
+  const int j_pad =
+      (kv_lim < a.Sk && (kv_lim % kBlockN) != 0 && kv_lim / kBlockN < n_tiles) ? kv_lim / kBlockN : -1;
 
   WaitCtl ctl{abort_flag, &g_status_word, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
 
@@ -180,7 +260,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
       mbar_init(bar_pv_done(q), 1);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_v_clean, 1);
     *abort_flag = 0u;
+    *reinterpret_cast<volatile uint32_t*>(gmisc + 8) = 0u;  // pad_issued
     fence_barrier_init();
     prefetch_tmap(&a.tm_q);
     prefetch_tmap(&a.tm_k);
@@ -221,6 +303,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(sKV + s * C::kTileBytes + c * C::kChunkBytes, m, bar_kv_full(s), c * 64,
                         kvh, j * kBlockN, b);
+          if (kind == 1 && j == j_pad) st_release_cta(pad_issued, 1u);
         }
         if (!ok) break;
       }
@@ -229,6 +312,18 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
       const int first = it > NSTAGE ? it - NSTAGE : 0;
       for (int i = first; i < it; ++i)
         mbar_wait_drain(bar_kv_full(i % NSTAGE), (i / NSTAGE) & 1, a.wait_limit_ns);
+    }
+  } else if (warp == C::kMmaWarp + 1) {
+    // ======================= padding rows of the tile straddling kv_len ====
+    if (j_pad >= 0) {
+      const int it_v = 2 * j_pad + 1;  // load index of V_{j_pad}
+      const bool ok = __all_sync(0xFFFFFFFFu, count_wait_sleep(pad_issued, 1u, ctl) &&
+                                                  mbar_wait(bar_kv_full(it_v % NSTAGE), (it_v / NSTAGE) & 1, ctl));
+      if (ok) {  // V tile landed; its stage is refilled only after O += P V of it
+        zero_padding_rows<D>(sKV + (it_v % NSTAGE) * C::kTileBytes, kv_lim % kBlockN, lane, 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_v_clean);
+      }
     }
   } else if (warp == C::kMmaWarp) {
     // ======================= MMA issuer ====================================
@@ -270,6 +365,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
           const uint32_t ph = (it / NSTAGE) & 1;
           ++it;
           if (!(ok = mbar_wait(bar_kv_full(s), ph, ctl))) break;
+          if (j == j_pad && !(ok = mbar_wait(bar_v_clean, 0, ctl))) break;  // padding rows zeroed
           H3_TRACE(kEvMmaV, j);
           tc_fence_after();
           const uint32_t vb = sKV + s * C::kTileBytes;

@@ -59,6 +59,7 @@
 //   warp 7     idle
 template <int D, int NSTAGE>
 struct PersistCfg {
+  static_assert(NSTAGE == 7 || NSTAGE == 12, "padding-row phase wait reasoned for these ring depths");
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kBlockM * D * 2;
   static constexpr int kChunkBytes = kBlockM * 128;
@@ -160,32 +161,6 @@ struct PipeCursor {
   }
 };
 
-// Shared-memory count: each producer thread adds with release, the waiter
-// reads with acquire (CTA scope).
-__device__ __forceinline__ void add_release_cta(uint32_t addr, uint32_t v) {
-  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_cta(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-// Wait until the count at addr reaches target; bounded like mbar_wait.
-__device__ __forceinline__ bool count_wait(uint32_t addr, uint32_t target, const WaitCtl& ctl) {
-  if (ld_acquire_cta(addr) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (ld_acquire_cta(addr) >= target) return true;
-    if (*ctl.abort_flag) return false;
-    if (globaltimer_ns() - t0 > ctl.limit_ns) {
-      *ctl.abort_flag = 1u;
-      atomicExch(ctl.status, ctl.timeout_code);
-      return false;
-    }
-  }
-}
 
 template <int D, int NSTAGE>
 __global__ void __launch_bounds__(256, 1) attn_persist_kernel(const __grid_constant__ AttnArgs a) {
@@ -232,6 +207,10 @@ __global__ void __launch_bounds__(256, 1) attn_persist_kernel(const __grid_const
   auto bpar = [](int J) { return static_cast<uint32_t>((J >> 1) & 1); };
 
   WaitCtl ctl{abort_flag, &g_status_word, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
+  int N = 0;  // key tiles in this CTA's stream
+  if (warp != C::kProducerWarp)
+    for (int i = 0; i < n_units; ++i) N += unit_at(i).n_tiles;
+  auto ld_v = [N](int J) { return min(J + 4, N) + J; };
 
   if (warp == C::kProducerWarp && lane == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
@@ -301,10 +280,7 @@ __global__ void __launch_bounds__(256, 1) attn_persist_kernel(const __grid_const
   } else if (warp == C::kMmaWarp || warp == C::kMmaWarp + 1) {
     // ======================= MMA issuers, one per tile parity ==============
     const int p = warp - C::kMmaWarp;
-    int N = 0;  // key tiles in this CTA's stream
-    for (int i = 0; i < n_units; ++i) N += unit_at(i).n_tiles;
     if (lane == 0 && N > p) {
-      auto ld_v = [N](int J) { return min(J + 4, N) + J; };
       auto ld_k = [](int J) { return J < 3 ? J : 2 * J - 3; };
       PipeCursor cq, cv;  // this thread's next Q K^T tile and next P V tile
       cq.start(&a, n_qb, n_units);
@@ -570,6 +546,15 @@ __global__ void __launch_bounds__(256, 1) attn_persist_kernel(const __grid_const
             break;
           }
           tc_fence_after();
+        }
+        if (w.kv_lim < a.Sk && kbase + kBlockN > w.kv_lim) {
+          // the tile straddles kv_len: zero V_J's padding rows once V_J has
+          // landed.  The stage's previous fill (K_J with 7 stages, V_{J-6}
+          // with 12) has landed by now, so this phase wait is exact.
+          const int ldv = ld_v(J);
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_kv_full(stage_of(ldv)), phase_of(ldv), ctl));
+          if (!ok) break;
+          zero_padding_rows<D>(sKV + stage_of(ldv) * C::kTileBytes, w.kv_lim - kbase, t, kBlockM);
         }
         tmem_st32(tP, pr[0]);
         tmem_st32(tP + 32, pr[1]);

@@ -28,15 +28,18 @@
 //   warps 0-3  softmax warpgroup, thread t = query row t = TMEM lane t
 //   warp 4     TMA producer: K_0, K_1, K_2, then K_{j+3}, V_j for j = 0, 1, ...
 //   warps 5-6  MMA issuers for even / odd key tiles (warp 5 allocates TMEM)
-//   warp 7     idle
+//   warp 7     padding: in the key tile that straddles kv_len, zeroes the V
+//              rows past kv_len (they may hold anything; 0 * NaN in O += P V
+//              would leak) before that tile's O += P V (barrier v_clean)
 template <int D, int NSTAGE>
 struct PipeCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kBlockM * D * 2;
   static constexpr int kChunkBytes = kBlockM * 128;
   static constexpr int kSmemKV = NSTAGE * kTileBytes;
-  // q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_read[2], p_ready[2], pv_done[2], drain[2]
-  static constexpr int kNumBars = 1 + 2 * NSTAGE + 10;
+  // q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_read[2], p_ready[2], pv_done[2], drain[2],
+  // v_clean
+  static constexpr int kNumBars = 1 + 2 * NSTAGE + 11;
   static constexpr int kSmemBytes = 1024 + kSmemKV + kNumBars * 8 + 16;
   static constexpr int kThreads = 256;
   static constexpr int kProducerWarp = 4;
@@ -73,9 +76,11 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   auto bar_p_ready = [&](int p) { return bars + 8u * (5 + 2 * NSTAGE + p); };
   auto bar_pv_done = [&](int p) { return bars + 8u * (7 + 2 * NSTAGE + p); };
   auto bar_drain = [&](int p) { return bars + 8u * (9 + 2 * NSTAGE + p); };
+  const uint32_t bar_v_clean = bars + 8u * (11 + 2 * NSTAGE);
   uint8_t* gmisc = gbase + C::kSmemKV + C::kNumBars * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gmisc + 4);
+  const uint32_t pad_issued = smem_u32(gmisc + 8);  // 1 once V of the tile straddling kv_len is requested
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -148,6 +153,21 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   };
   // Tile j's barriers of parity j % 2 complete for the (j / 2)-th time.
   auto bpar = [](int j) { return static_cast<uint32_t>((j >> 1) & 1); };
+  // Iteration of the key tile that straddles kv_len (keys from kv_len on are
+  // padding, read into the tile but never attended), or -1: none is loaded,
+  // or kv_len is Sk or a tile edge.
+  int j_pad = -1;
+  if (n_tiles > 0 && kv_lim < a.Sk && (kv_lim % kBlockN) != 0) {
+    const int tb = kv_lim / kBlockN;
+    int m = -1;  // position of tile tb in the CTA's tile list
+    if constexpr (WIN) {
+      if (tb < n_lead) m = tb;
+      else if (tb >= mid0 && tb < mid0 + n_tiles - n_lead) m = n_lead + (tb - mid0);
+    } else {
+      if (tb < n_tiles) m = tb;
+    }
+    if (m >= 0) j_pad = m >= rot ? m - rot : m - rot + n_tiles;
+  }
 
   WaitCtl ctl{abort_flag, &g_status_word, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
 
@@ -164,7 +184,9 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       mbar_init(bar_pv_done(p), 1);
       mbar_init(bar_drain(p), 1);
     }
+    mbar_init(bar_v_clean, 1);
     *abort_flag = 0u;
+    *reinterpret_cast<volatile uint32_t*>(gmisc + 8) = 0u;  // pad_issued
     fence_barrier_init();
     prefetch_tmap(&a.tm_k);
     prefetch_tmap(&a.tm_v);
@@ -192,6 +214,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_4d(sKV + s * C::kTileBytes + c * C::kChunkBytes, m, bar_kv_full(s), c * 64, kvh,
                       tile_of(j) * kBlockN, b);
+        if (kind == 1 && j == j_pad) st_release_cta(pad_issued, 1u);
         ++ld;
       };
       for (int j = 0; ok && j < 3 && j < n_tiles; ++j) load(0, j);
@@ -237,6 +260,8 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
         if (!(ok = mbar_wait(bar_kv_full(sv), phase_of(ldv), ctl))) break;
         H3_TRACE(kEvMmaV, j);
         if (!(ok = mbar_wait(bar_p_ready(p), bpar(j), ctl))) break;
+        // V_j's padding rows are zeroed (warp 7)
+        if (j == j_pad && !(ok = mbar_wait(bar_v_clean, 0, ctl))) break;
         H3_TRACE(kEvMmaPV0, j);
         tc_fence_after();
         const uint32_t vb = sKV + sv * C::kTileBytes;
@@ -253,6 +278,18 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       // Drain every MMA issued by this thread before tensor memory is freed.
       tc_commit(bar_drain(p));
       mbar_wait_drain(bar_drain(p), 0, a.wait_limit_ns);
+    }
+  } else if (warp == 7) {
+    // ======================= padding rows of the tile straddling kv_len ====
+    if (j_pad >= 0) {
+      const int ldv = ld_v(j_pad), sv = stage_of(ldv);
+      const bool ok = __all_sync(0xFFFFFFFFu, count_wait_sleep(pad_issued, 1u, ctl) &&
+                                                  mbar_wait(bar_kv_full(sv), phase_of(ldv), ctl));
+      if (ok) {  // V tile landed; its stage is refilled only after O += P V of it
+        zero_padding_rows<D>(sKV + sv * C::kTileBytes, kv_lim % kBlockN, lane, 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_v_clean);
+      }
     }
   } else if (warp < 4) {
     // ======================= softmax / correction / epilogue ===============
