@@ -462,20 +462,26 @@ def _time_window(h3, gen, torch, stream, peaks, steps=5, warmup=3):
 
 
 # The library's choice of attention kernel: one query tile per CTA (Q held in
-# tensor memory) from 1024 keys on, for head dims 64 and 128; two query tiles
-# per CTA otherwise.  H3ATTN_ATTN_KERNEL=1/2 forces one or the other; 3 the
-# persistent one-CTA-per-SM kernel (head dims 64 and 128).
+# tensor memory) for head dim 128 from 1024 keys on; one query tile per CTA
+# with two CTAs per SM for head dim 128 below that and for head dim 64; the
+# two-tile kernel's code with one tile for head dim 256.  H3ATTN_ATTN_KERNEL
+# forces 1 (one tile, Q in tensor memory), 2 (two tiles per CTA), 3 (the
+# persistent kernel) or 4 (two CTAs per SM) where the head dim has it.
 ONE_TILE_MIN_KEYS = 1024
 
 
 def _attn_kernel_name(wl):
     sel = os.environ.get("H3ATTN_ATTN_KERNEL", "")
-    if sel == "3" and wl.D in (64, 128):
+    if wl.D == 256:
+        return "attn_fwd_kernel<256,1,2,1>"
+    if sel == "3":
         return {64: "attn_persist_kernel<64,12>", 128: "attn_persist_kernel<128,7>"}[wl.D]
-    one_tile = wl.D in (64, 128) and (sel == "1" or (sel != "2" and wl.Sk >= ONE_TILE_MIN_KEYS))
+    one_tile = sel == "1" or (sel not in ("2", "4") and wl.D == 128 and wl.Sk >= ONE_TILE_MIN_KEYS)
     if one_tile:
         return {64: "attn_pipe_kernel<64,12>", 128: "attn_pipe_kernel<128,7>"}[wl.D]
-    return {64: "attn_fwd_kernel<64,2,8>", 128: "attn_fwd_kernel<128,2,4>", 256: "attn_fwd_kernel<256,1,2>"}[wl.D]
+    if sel == "2":
+        return {64: "attn_fwd_kernel<64,2,8,1>", 128: "attn_fwd_kernel<128,2,4,1>"}[wl.D]
+    return {64: "attn_fwd_kernel<64,1,4,2>", 128: "attn_fwd_kernel<128,1,2,2>"}[wl.D]
 
 
 def _profiled_traffic():

@@ -149,9 +149,10 @@ h3attn_status_t h3attn_qk_norm_rope_out(const void* q, const void* k, void* q_ou
  *    causal mask to every sample; causal masking requires Sq == Sk.
  * D in {64, 128, 256}; Hq % Hkv == 0; B, Sq, Sk, Hq, Hkv >= 1 (B*Sq == 0 is
  * a no-op); B, Hq <= 65535 and ceil(Sq/128)*Hq*B < 2^31 (work units).
- * Scheduling: a work unit is 128 (D 64/128, from 1024 keys on) or 256 query
- * rows of one batch item and head; the units are launched longest (causal)
- * first and the hardware places them on the SMs as they free up.
+ * Scheduling: a work unit is 128 query rows of one batch item and head; the
+ * units are launched longest (causal) first and the hardware places them on
+ * the SMs as they free up (one resident CTA per SM for head dim 128 from 1024
+ * keys on, two otherwise).
  * Accumulation is float32 on the tensor cores; softmax in float32
  * with exp2; the output is rounded once to bf16.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_HEAD_DIM, UNSUPPORTED_DEVICE,

@@ -42,9 +42,10 @@ def full_case(h3, B, Sq, Sk, Hq, Hkv, D, seed=0, causal=False, kv_len=None, q_le
 # ---------------------------------------------------------------- small / edge cases
 # Every edge case runs on every attention kernel: "1" = one query tile per CTA
 # (Q in tensor memory), "2" = two query tiles per CTA, "3" = the persistent
-# kernel (one CTA per SM over all units; head_dim 256 falls back to "2").
-# Without the override the library picks by key length.
-@pytest.fixture(params=["1", "2", "3"], ids=["one_tile", "two_tiles", "persistent"])
+# kernel (one CTA per SM over all units), "4" = one query tile per CTA, two
+# CTAs per SM (head_dim 256 falls back to "2" for "3" and "4").  Without the
+# override the library picks by key length.
+@pytest.fixture(params=["1", "2", "3", "4"], ids=["one_tile", "two_tiles", "persistent", "two_ctas"])
 def kernel(request, monkeypatch):
     monkeypatch.setenv("H3ATTN_ATTN_KERNEL", request.param)
     return request.param

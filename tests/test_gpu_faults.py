@@ -12,7 +12,7 @@ from helpers import check_close, from_dev, to_dev
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("kernel", ["1", "2", "3"], ids=["one_tile", "two_tiles", "persistent"])
+@pytest.mark.parametrize("kernel", ["1", "2", "3", "4"], ids=["one_tile", "two_tiles", "persistent", "two_ctas"])
 def test_stalled_producer_times_out_and_context_survives(h3, monkeypatch, kernel):
     import torch
     B, S, H, D = 1, 256, 1, 128  # one CTA: one wait limit of runtime

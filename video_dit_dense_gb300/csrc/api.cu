@@ -241,9 +241,9 @@ h3attn_status_t prefill(const void* q, const void* k, const void* v, void* o, in
   a.wait_limit_ns = wait_limit_ns();
   const char* inj = getenv("H3ATTN_FAULT_INJECT_STALL_PRODUCER");
   a.debug_skip_producer = (inj && inj[0] == '1') ? 1 : 0;
-  // Kernel choice override (tests run every case on every kernel): "1", "2" or "3".
+  // Kernel choice override (tests run every case on every kernel): "1" .. "4".
   const char* kern = getenv("H3ATTN_ATTN_KERNEL");
-  a.kernel = (kern && kern[0] >= '1' && kern[0] <= '3') ? kern[0] - '0' : 0;
+  a.kernel = (kern && kern[0] >= '1' && kern[0] <= '4') ? kern[0] - '0' : 0;
   a.win_ct = a.win_af = a.win_r = 0;
   if (win) {
     a.kernel = 1;  // the window's tile ranges live in the one-query-tile kernel

@@ -50,7 +50,10 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max
 // tile by 2^kRescaleThreshold: no score exceeds the running max by more.
 constexpr float kFastPassSumLimit = 256.0f;
 
-template <int D, int NQ, int NSTAGE>
+// CTAS: resident CTAs per SM the configuration is built for (1, or 2 for one
+// query tile with a short ring: one CTA's prologue and epilogue then overlap
+// the other's products).
+template <int D, int NQ, int NSTAGE, int CTAS = 1>
 struct Cfg {
   static constexpr int kChunks = D / 64;                  // 128-byte swizzle columns per row
   static constexpr int kTileBytes = kBlockM * D * 2;      // one 128-row tile of Q, K or V
@@ -63,10 +66,10 @@ struct Cfg {
   static constexpr int kThreads = NQ * 128 + 128;
   static constexpr int kProducerWarp = NQ * 4;
   static constexpr int kMmaWarp = NQ * 4 + 1;
-  // Register split: launch budget kThreads * floor(65536 / kThreads) (rounded to 8);
+  // Register split: launch budget kThreads * floor(65536 / (kThreads * CTAS)) (rounded to 8);
   // the control warpgroup drops to kCtlRegs, softmax warpgroups rise to kSoftRegs.
-  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
-  static constexpr int kCtlRegs = 96;
+  static constexpr int kLaunchRegs = (65536 / (kThreads * CTAS)) / 8 * 8;
+  static constexpr int kCtlRegs = CTAS == 1 ? 96 : 56;
   static constexpr int kSoftRegs =
       ((kThreads * kLaunchRegs - 128 * kCtlRegs) / (NQ * 128)) / 8 * 8 > 232
           ? 232
@@ -77,8 +80,11 @@ struct Cfg {
   static constexpr int kColO = NQ * 128;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kBlockN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
-  static_assert(kColO + NQ * D <= static_cast<int>(kTmemCols), "tensor memory budget");
+  // tensor memory per CTA: all of it, or an equal share (a power of two >= 32 columns)
+  static constexpr uint32_t kTmemAlloc = CTAS == 1 ? kTmemCols : kTmemCols / CTAS;
+  static_assert(kColO + NQ * D <= static_cast<int>(kTmemAlloc), "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(CTAS * (kSmemBytes + 1024) <= 233472, "shared memory of CTAS resident CTAs");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -196,10 +202,10 @@ __device__ unsigned long long g_trace[kNumEv][kTraceTiles];
   } while (0)
 #endif
 
-template <int D, int NQ, int NSTAGE>
-__global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
+template <int D, int NQ, int NSTAGE, int CTAS>
+__global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
     attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
-  using C = Cfg<D, NQ, NSTAGE>;
+  using C = Cfg<D, NQ, NSTAGE, CTAS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -269,7 +275,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
     prefetch_tmap(&a.tm_v);
   }
   if (warp == C::kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemAlloc);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -543,17 +549,17 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE>::kThreads, 1)
   __syncthreads();
   if (warp == C::kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemAlloc);
   }
 }
 
 #include "attn_pipe.cuh"
 #include "attn_persist.cuh"
 
-template <int D, int NQ, int NSTAGE>
+template <int D, int NQ, int NSTAGE, int CTAS = 1>
 cudaError_t launch_cfg(const AttnArgs& a, cudaStream_t stream) {
-  using C = Cfg<D, NQ, NSTAGE>;
-  auto kern = attn_fwd_kernel<D, NQ, NSTAGE>;
+  using C = Cfg<D, NQ, NSTAGE, CTAS>;
+  auto kern = attn_fwd_kernel<D, NQ, NSTAGE, CTAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int rows_per_cta = NQ * kBlockM;
@@ -597,20 +603,31 @@ int read_and_clear_status(int* value) {
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
-  // Two kernels for head_dim 64/128: one query tile per CTA with Q in tensor
-  // memory and two MMA-issuing threads (faster from about a thousand keys
-  // on), or two query tiles per CTA sharing each K/V tile (faster on short
-  // key ranges, where its shorter prologue matters).  a.kernel: 0 = by key
-  // length, 1 = one query tile, 2 = two query tiles, 3 = the persistent
-  // kernel (one CTA per SM over all units; head_dim 64/128, not windowed).
+  // Kernels (measured on GB300 with the workloads' shapes):
+  //   1  one 128-row query tile per CTA, Q in tensor memory, two MMA-issuing
+  //      threads, 7-stage ring (12 for head_dim 64): head_dim 128 from 1024
+  //      keys on, and the chunked window;
+  //   4  the two-tile kernel's code with one query tile per CTA, a short ring
+  //      and two CTAs per SM (one CTA's prologue and epilogue overlap the
+  //      other's products): head_dim 128 below 1024 keys, head_dim 64;
+  //   2  two query tiles per CTA sharing each K/V tile: head_dim 256 (one
+  //      tile per CTA there), otherwise only on request;
+  //   3  the persistent kernel (one CTA per SM over all units), on request.
+  // a.kernel: 0 = by shape, else the kernel above (head dims it lacks fall
+  // back to the shape rule's next choice).
   if (a.kernel == 3 && a.win_ct == 0) {
     if (a.D == 64) return launch_persist<64, 12>(a, stream);
     if (a.D == 128) return launch_persist<128, 7>(a, stream);
   }
-  const bool one_tile = a.kernel == 1 || (a.kernel == 0 && a.Sk >= kOneTileMinKeys);
+  const bool one_tile = a.kernel == 1 || (a.kernel == 0 && a.D == 128 && a.Sk >= kOneTileMinKeys);
+  const bool two_ctas = !one_tile && a.win_ct == 0 && (a.kernel == 4 || a.kernel == 0);
   switch (a.D) {
-    case 64: return one_tile ? launch_pipe<64, 12>(a, stream) : launch_cfg<64, 2, 8>(a, stream);
-    case 128: return one_tile ? launch_pipe<128, 7>(a, stream) : launch_cfg<128, 2, 4>(a, stream);
+    case 64:
+      return one_tile ? launch_pipe<64, 12>(a, stream)
+                      : (two_ctas ? launch_cfg<64, 1, 4, 2>(a, stream) : launch_cfg<64, 2, 8>(a, stream));
+    case 128:
+      return one_tile ? launch_pipe<128, 7>(a, stream)
+                      : (two_ctas ? launch_cfg<128, 1, 2, 2>(a, stream) : launch_cfg<128, 2, 4>(a, stream));
     case 256: return launch_cfg<256, 1, 2>(a, stream);
     default: return cudaErrorInvalidValue;
   }
