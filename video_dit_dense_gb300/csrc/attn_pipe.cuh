@@ -89,7 +89,10 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   const int b = blockIdx.z;
   const int h = blockIdx.y;
   const int kvh = h / (a.Hq / a.Hkv);
-  const int qb = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // longest (causal) first
+  // Longest units first: with a causal mask the last query blocks; under the
+  // chunked window the first ones (blocks holding anchor rows see every key,
+  // and the last chunk's window is cut at the sequence end).
+  const int qb = WIN ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
   const int q0 = qb * kBlockM;
   int kv_lim = a.Sk;
   if (a.kv_len) kv_lim = min(kv_lim, max(a.kv_len[b], 0));
