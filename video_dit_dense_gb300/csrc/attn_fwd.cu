@@ -14,6 +14,8 @@
 //                  tcgen05.mma (both operands in shared memory, fp32
 //                  accumulator in tensor memory), then O_q += P_q V_j with
 //                  P_q read from tensor memory.  Also allocates tensor memory.
+//   warp 4*NQ+2    zeroes the V rows past kv_len of the key tile that
+//                  straddles kv_len, before that tile's O += P V.
 //   warps 4q..4q+3 softmax warpgroup of tile q: thread t owns query row t
 //                  (tensor-memory lane t).  It reads its 128 scores, applies
 //                  the mask, keeps a running max and sum, writes
@@ -21,9 +23,9 @@
 //                  memory over the scores, rescales its O row when the max
 //                  grows by more than 2^8, and finally writes O / l.
 //
-// Tensor memory (512 columns x 128 lanes): S_q at columns [128q, 128q+128),
-// P_q over the first 64 columns of S_q (bf16 pairs), O_q at
-// [128*NQ + D*q, 128*NQ + D*(q+1)).
+// Tensor memory (128 lanes; all 512 columns, or 256 when two CTAs share an
+// SM): S_q at columns [128q, 128q+128), P_q over the first 64 columns of S_q
+// (bf16 pairs), O_q at [128*NQ + D*q, 128*NQ + D*(q+1)).
 //
 // The next S_q = Q_q K^T overwrites P_q, and tcgen05 only orders MMAs that
 // share an accumulator, so the issuer waits for O_q += P_q V to complete
@@ -62,7 +64,8 @@ struct Cfg {
   static constexpr int kSmemKV = NSTAGE * kTileBytes;
   static constexpr int kNumBars = 1 + 2 * NSTAGE + 3 * NQ + 2;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kSmemQ + kSmemKV + kNumBars * 8 + 16;
-  // NQ softmax warpgroups + one control warpgroup (producer, MMA issuer, two idle warps)
+  // NQ softmax warpgroups + one control warpgroup (producer, MMA issuer, the warp that zeroes V
+  // padding rows, one idle warp)
   static constexpr int kThreads = NQ * 128 + 128;
   static constexpr int kProducerWarp = NQ * 4;
   static constexpr int kMmaWarp = NQ * 4 + 1;
