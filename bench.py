@@ -53,6 +53,25 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(values, ws, device):
+    """Element-wise max of this rank's timings over all ranks (the slowest rank
+    sets each time); a no-op on one rank.  `device` is where the process
+    group's collectives run ("cuda" for NCCL, "cpu" for gloo)."""
+    if ws <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(ws, units_per_step, steps, total_ms):
+    """Whole-job throughput: every rank processes units_per_step per step (weak
+    scaling), and the slowest rank's time counts."""
+    return ws * units_per_step * steps / (total_ms * 1e-3)
+
+
 def _allowed_pairs(wl, kv_len, causal_b):
     """Allowed (query row, key) pairs summed over samples (structured masks)."""
     total = 0
@@ -283,17 +302,14 @@ def run_gpu(args):
     mod = _time_rmsnorm_modulate(h3, gen, torch, stream, peaks) if args.modulate else None
     wnd = _time_window(h3, gen, torch, stream, peaks) if args.window else None
 
-    times = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
-    if ws > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = times.tolist()
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], ws, "cuda")
     if rank != 0:
         if ws > 1:
             dist.destroy_process_group()
         return
 
     ms_per_step = total_ms / args.steps
-    value = ws * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(ws, flops, args.steps, total_ms) / 1e12
     attn_tflops = flops / (attn_ms * 1e-3) / 1e12
     norm_gbs = norm_bytes / (norm_ms * 1e-3) / 1e9 if wl.norm_rope else None
     # recorded traffic is for the default workload's launches only
@@ -330,7 +346,7 @@ def run_gpu(args):
         "e2e": {
             "how": "per step: H2D of q,k,v from pinned host memory, both kernels, D2H of o; "
                    "two buffer sets, copies of neighbouring steps overlap kernels on separate streams",
-            "value": round(ws * flops * args.steps / (e2e_ms * 1e-3) / 1e12, 2),
+            "value": round(job_throughput(ws, flops, args.steps, e2e_ms) / 1e12, 2),
             "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
             "d2h_bytes_per_step": int(ho.numel() * 2),
