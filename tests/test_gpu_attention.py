@@ -76,15 +76,16 @@ def test_causal_and_padding(h3, kernel, D):
 
 
 @pytest.mark.gpu
-def test_bit_mask_and_q_len_and_degenerate(h3, kernel):
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_bit_mask_and_q_len_and_degenerate(h3, kernel, D):
     # random packed boolean [Q, K] mask, combined with key padding
-    full_case(h3, 2, 200, 333, 2, 2, 128, seed=5, bits_density=0.3, kv_len=np.array([333, 100], np.int32),
-              what="bits+pad")
+    full_case(h3, 2, 200, 333, 2, 2, D, seed=5, bits_density=0.3, kv_len=np.array([333, 100], np.int32),
+              what=f"bits+pad D={D}")
     # very sparse mask: many rows fully masked -> zero rows
-    full_case(h3, 1, 140, 140, 2, 2, 128, seed=6, bits_density=0.002, what="sparse bits")
+    full_case(h3, 1, 140, 140, 2, 2, D, seed=6, bits_density=0.002, what=f"sparse bits D={D}")
     # zero-tail mode and kv_len <= 0 (every key masked -> zeros)
-    full_case(h3, 3, 270, 270, 2, 2, 128, seed=7, q_len=np.array([270, 13, 0], np.int32),
-              kv_len=np.array([-5, 270, 100], np.int32), what="q_len/kv_len edge")
+    full_case(h3, 3, 270, 270, 2, 2, D, seed=7, q_len=np.array([270, 13, 0], np.int32),
+              kv_len=np.array([-5, 270, 100], np.int32), what=f"q_len/kv_len edge D={D}")
 
 
 @pytest.mark.gpu
