@@ -159,3 +159,33 @@ def test_prefill_window_validation(lib):
     assert window_call(lib, q=FAKE + 8) == h3.H3ATTN_ERR_MISALIGNED
     assert window_call(lib, o=FAKE) == h3.H3ATTN_ERR_INVALID_ARG                 # o aliases q
     assert window_call(lib, S=0) == h3.H3ATTN_OK
+
+
+def test_binding_rejects_bad_python_arguments(lib):
+    """The binding's own checks answer with H3AttnError before any CUDA call
+    (CPU tensors are never accepted as device buffers)."""
+    import torch
+    with pytest.raises(h3.H3AttnError, match="at least one of q and k"):
+        h3.h3attn_qk_norm_rope(None, None, None, None, None, None)
+    cpu = torch.zeros(1, 4, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(h3.H3AttnError, match="CUDA tensor"):
+        h3.h3attn_qk_norm_rope(cpu, None, None, None, None, None)
+    with pytest.raises(h3.H3AttnError, match="CUDA tensor"):
+        h3.h3attn_prefill(cpu, cpu, cpu, cpu)
+    with pytest.raises(h3.H3AttnError, match="CUDA tensor"):
+        h3.h3attn_rmsnorm_modulate(cpu[0, :, 0], cpu[0, :, 0], None, cpu[0, :, 0], cpu[0, :, 0])
+    with pytest.raises(h3.H3AttnError, match="inference only"):
+        h3._check_bf16("q", _GradEnabledBf16())
+
+
+class _GradEnabledBf16:
+    """Stands in for a contiguous 4-D bf16 CUDA tensor that requires grad."""
+    dtype = __import__("torch").bfloat16
+    is_cuda = True
+    requires_grad = True
+
+    def is_contiguous(self):
+        return True
+
+    def dim(self):
+        return 4

@@ -143,3 +143,26 @@ def test_out_of_place_edge_shapes_and_alias(h3, D, rot, B, S, Hq, Hkv):
     gq, gk, _, _ = _run_out(h3, q, k, w, w, cos, sin, rot, 1e-6, alias=True)
     _assert_bits_equal(gq, eq, "aliased q")
     _assert_bits_equal(gk, ek, "aliased k")
+
+
+@pytest.mark.gpu
+def test_binding_rejects_short_weights_and_missing_tables(h3):
+    """Arguments the kernel would read past (a weight vector shorter than D,
+    absent RoPE tables, a strided per-sample length vector) are refused by the
+    binding before any launch, and the device status stays clean."""
+    import torch
+    q = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(128, dtype=torch.float32, device="cuda")
+    cos = torch.ones(8, 48, dtype=torch.float32, device="cuda")
+    with pytest.raises(h3.H3AttnError, match="wq must be"):
+        h3.h3attn_qk_norm_rope(q, None, w[:64], None, cos, cos)
+    with pytest.raises(h3.H3AttnError, match="cos and sin are required"):
+        h3.h3attn_qk_norm_rope(q, None, w, None, None, None, rotary_dim=96)
+    h3.h3attn_qk_norm_rope(q, None, w, None, None, None, rotary_dim=0)   # no rotation: no tables needed
+    q2 = torch.zeros(2, 8, 2, 128, dtype=torch.bfloat16, device="cuda")
+    kv_len = torch.full((4,), 8, dtype=torch.int32, device="cuda")[::2]    # [2], stride 2
+    with pytest.raises(h3.H3AttnError, match="kv_len must be"):
+        h3.h3attn_prefill_window(q2, q2, q2, torch.empty_like(q2), h3.Window(4, 0, 1, 0),
+                                 mask=h3.Mask(kv_len=kv_len))
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0

@@ -140,6 +140,8 @@ def _raise_if(status, where):
 
 
 def _norm_rope_args(q, k, wq, wk, cos, sin, rotary_dim):
+    if q is None and k is None:
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "at least one of q and k must be given")
     ref = q if q is not None else k
     if q is not None:
         _check_bf16("q", q)
@@ -154,9 +156,15 @@ def _norm_rope_args(q, k, wq, wk, cos, sin, rotary_dim):
     for name, t in (("wq", wq), ("wk", wk), ("cos", cos), ("sin", sin)):
         if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()):
             raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must be a contiguous float32 CUDA tensor")
-    if rotary_dim > 0 and (cos.shape[-1] != rotary_dim // 2 or cos.numel() < S * (rotary_dim // 2)
-                           or sin.shape != cos.shape):
-        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "cos/sin must be [>=S, rotary_dim/2]")
+    # the kernel reads D weights per row: a shorter tensor would be read past its end
+    for name, rows, w in (("wq", q, wq), ("wk", k, wk)):
+        if rows is not None and (w is None or w.numel() != D):
+            raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must be a [{D}] float32 CUDA tensor")
+    if rotary_dim > 0:
+        if cos is None or sin is None:
+            raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "cos and sin are required when rotary_dim > 0")
+        if cos.shape[-1] != rotary_dim // 2 or cos.numel() < S * (rotary_dim // 2) or sin.shape != cos.shape:
+            raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "cos/sin must be [>=S, rotary_dim/2]")
     return B, S, Hq, Hkv, D
 
 
@@ -202,6 +210,17 @@ class Mask:
     bits: object = None      # int32/uint32 [B, Sq, ceil(Sk/32)]
 
 
+def _mask_struct(mask: Mask, B: int):
+    """Checks the per-sample fields of a mask and packs its pointers into an
+    h3attn_mask_t (the kernels read B entries of each field given)."""
+    import torch
+    for name, t, dt in (("kv_len", mask.kv_len, torch.int32), ("q_len", mask.q_len, torch.int32),
+                        ("causal_b", mask.causal_b, torch.uint8)):
+        if t is not None and (t.dtype != dt or t.numel() != B or not t.is_cuda or not t.is_contiguous()):
+            raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must be a contiguous [{B}] {dt} CUDA tensor")
+    return ctypes.pointer(h3attn_mask_t(_ptr(mask.kv_len), _ptr(mask.q_len), _ptr(mask.causal_b), _ptr(mask.bits)))
+
+
 def h3attn_prefill(q, k, v, o, scale=None, mask: Mask | None = None, causal=False, stream=None):
     """o <- softmax(q k^T * scale) v on BSHD bf16 tensors (o preallocated)."""
     load()
@@ -215,19 +234,15 @@ def h3attn_prefill(q, k, v, o, scale=None, mask: Mask | None = None, causal=Fals
         scale = 1.0 / float(D) ** 0.5
     mptr = None
     if mask is not None:
-        import torch
         if mask.bits is not None:
             if mask.bits.dim() == 4:
                 raise H3AttnError(H3ATTN_ERR_UNSUPPORTED_MASK, "per-head [B, H, Q, K] masks are not supported")
             W = (Sk + 31) // 32
-            if tuple(mask.bits.shape) != (B, Sq, W) or mask.bits.element_size() != 4:
-                raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"bits must be 32-bit words of shape [{B}, {Sq}, {W}]")
-        for name, t, dt in (("kv_len", mask.kv_len, torch.int32), ("q_len", mask.q_len, torch.int32),
-                            ("causal_b", mask.causal_b, torch.uint8)):
-            if t is not None and (t.dtype != dt or t.numel() != B or not t.is_cuda):
-                raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"{name} must be a [{B}] {dt} CUDA tensor")
-        m = h3attn_mask_t(_ptr(mask.kv_len), _ptr(mask.q_len), _ptr(mask.causal_b), _ptr(mask.bits))
-        mptr = ctypes.pointer(m)
+            if tuple(mask.bits.shape) != (B, Sq, W) or mask.bits.element_size() != 4 or \
+                    not mask.bits.is_cuda or not mask.bits.is_contiguous():
+                raise H3AttnError(H3ATTN_ERR_INVALID_ARG,
+                                  f"bits must be contiguous 32-bit CUDA words of shape [{B}, {Sq}, {W}]")
+        mptr = _mask_struct(mask, B)
     st = _lib.h3attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Sq, Sk, Hq, Hkv, D, float(scale), mptr,
                              int(bool(causal)), _stream_handle(stream))
     _raise_if(st, "h3attn_prefill")
@@ -283,8 +298,7 @@ def h3attn_prefill_window(q, k, v, o, window: Window, scale=None, mask: Mask | N
     if mask is not None:
         if mask.bits is not None or mask.causal_b is not None:
             raise H3AttnError(H3ATTN_ERR_UNSUPPORTED_MASK, "the window combines with kv_len / q_len only")
-        m = h3attn_mask_t(_ptr(mask.kv_len), _ptr(mask.q_len), None, None)
-        mptr = ctypes.pointer(m)
+        mptr = _mask_struct(mask, B)
     w = h3attn_window_t(int(window.frame_tokens), int(window.anchor_frames), int(window.chunk_frames),
                         int(window.radius))
     st = _lib.h3attn_prefill_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, S, Hq, k.shape[2], D, float(scale),
