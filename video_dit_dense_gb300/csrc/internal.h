@@ -15,7 +15,7 @@ int read_and_clear_status(int* value);
 // Device address of the current device's status word (nullptr on failure).
 int* status_word_ptr();
 
-// ---- fused Q/K RMSNorm + bf16 boundary + partial RoPE (in place) ----
+// ---- fused Q/K RMSNorm + bf16 boundary + partial RoPE (in place or out of place) ----
 // Division of 32-bit unsigned integers by a runtime constant d with one
 // 64x64 multiply-high: q = floor(M * n / 2^64), M = floor((2^64 - 1) / d) + 1,
 // exact for every 32-bit n (Lemire, Kaser and Kurz, "Faster remainder by
@@ -85,7 +85,9 @@ struct AttnArgs {
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int debug_skip_producer;  // fault injection for the bounded-wait test: 1 = never load K/V
-  int kernel;               // 0 = choose by key length, 1 = one query tile per CTA, 2 = two
+  // 0 = choose by head dim and key length; 1 = one query tile per CTA (Q in tensor memory),
+  // 2 = two query tiles per CTA, 3 = persistent (one CTA per SM), 4 = one query tile, two CTAs per SM
+  int kernel;
   // chunked window (self-attention, one-query-tile kernel only): tokens per
   // chunk (0 = dense), anchor tokens, radius in chunks
   int win_ct, win_af, win_r;
