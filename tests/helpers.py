@@ -70,3 +70,17 @@ def sample_rows(B, Sq, Hq, per_head, seed, kv_len=None, causal_b=None, extra_row
             for i in rows:
                 ids.append((b * Sq + i) * Hq + h)
     return np.array(sorted(set(ids)), dtype=np.int64)
+
+
+def assert_convex_bound(dv, do, group: int, what: str):
+    """A property of every output element, at any size (checked on the
+    device): an attention output row is a softmax-weighted average of value
+    rows (or zero), so it is finite and |o[b,i,h,d]| <= max_j |v[b,j,h//group,d]|,
+    up to the bf16 rounding of P and of o (a relative slack of 1 %)."""
+    import torch
+    o = do.float()
+    assert bool(torch.isfinite(o).all()), f"{what}: non-finite outputs"
+    vmax = dv.float().abs().amax(dim=1)                          # [B, Hkv, D]
+    bound = vmax.repeat_interleave(group, dim=1)[:, None]        # [B, 1, Hq, D]
+    over = o.abs() > bound * 1.01 + 1e-6
+    assert not bool(over.any()), f"{what}: {int(over.sum())} outputs exceed the value range of their column"

@@ -8,7 +8,8 @@ import pytest
 
 import h3inputs as gen
 import oracle
-from helpers import (check_close, from_dev, sample_rows, to_dev, to_dev_f32, to_dev_i32, to_dev_u8)
+from helpers import (assert_convex_bound, check_close, from_dev, sample_rows, to_dev, to_dev_f32, to_dev_i32,
+                     to_dev_u8)
 
 
 def gpu_attention(h3, q, k, v, scale, causal=False, kv_len=None, q_len=None, causal_b=None, bits=None):
@@ -158,7 +159,9 @@ def _gpu_step(h3, wl, inp):
     h3.h3attn_prefill(dq, dk, dv, do, wl.scale, mask, False)
     torch.cuda.synchronize()
     assert h3.h3attn_check_device_status() == 0
+    assert_convex_bound(dv, do, wl.Hq // wl.Hkv, wl.name)
     return from_dev(do)
+
 
 
 FULL = ["tiny_mha", "dit_block", "padded_gqa_d64", "padded_gqa_d256"]

@@ -9,7 +9,7 @@ import pytest
 
 import h3inputs as gen
 import oracle
-from helpers import check_close, from_dev, sample_rows, to_dev, to_dev_i32
+from helpers import assert_convex_bound, check_close, from_dev, sample_rows, to_dev, to_dev_i32
 
 
 def gpu_window(h3, q, k, v, scale, win, kv_len=None, q_len=None):
@@ -23,6 +23,7 @@ def gpu_window(h3, q, k, v, scale, win, kv_len=None, q_len=None):
     h3.h3attn_prefill_window(dq, dk, dv, do, h3.Window(*win), scale, mask)
     torch.cuda.synchronize()
     assert h3.h3attn_check_device_status() == 0
+    assert_convex_bound(dv, do, dq.shape[2] // dk.shape[2], "window")   # every row written, none out of range
     return from_dev(do)
 
 
