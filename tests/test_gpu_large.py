@@ -1,0 +1,70 @@
+"""Tensors past 2^31 elements (byte offsets past 2^32): the norm/RoPE kernel
+and the attention kernels the library picks for head dim 128 (one query tile
+per CTA; two CTAs per SM), on a cross-attention shape whose query has
+2^31 + 4.2 M elements (4.3 GB per tensor), compared with the oracle on sampled
+rows on both sides of the 2^31-element line.  Only the sampled rows come back
+to the host."""
+import numpy as np
+import pytest
+
+import h3inputs as gen
+import oracle
+from helpers import assert_convex_bound, check_close, sample_rows, to_dev, to_dev_f32
+
+B, SQ, SK, H, D = 1, (1 << 21) + 4133, 128 + 77, 8, 128
+ROT, EPS = 96, 1e-6
+LINE = (1 << 31) // (H * D)   # first token whose rows start past 2^31 elements
+
+
+@pytest.fixture(scope="module")
+def big_inputs():
+    q = gen.normal_bshd(B, SQ, H, D, 21, gen.STREAM_Q)
+    k = gen.normal_bshd(B, SK, H, D, 21, gen.STREAM_K)
+    v = gen.normal_bshd(B, SK, H, D, 21, gen.STREAM_V)
+    assert q.size > (1 << 31)
+    return q, k, v
+
+
+def _rows_back(t, ids):
+    """The sampled (token, head) rows of a BSHD device tensor, as bf16 bits on the host."""
+    import torch
+    sel = t.view(-1, D)[torch.from_numpy(ids).cuda()]
+    return sel.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.gpu
+def test_norm_rope_past_2_to_the_31_elements(h3, big_inputs):
+    import torch
+    q, _, _ = big_inputs
+    w = gen.uniform_f32(D, 21, gen.STREAM_WQ, 0.5, 1.5)
+    cos, sin = gen.rope_tables(SQ, ROT)
+    dq = to_dev(q)
+    dq_out = torch.empty_like(dq)
+    h3.h3attn_qk_norm_rope_out(dq, None, dq_out, None, to_dev_f32(w), None, to_dev_f32(cos), to_dev_f32(sin),
+                               ROT, EPS)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    for s0, s1 in ((0, 64), (LINE - 40, LINE + 40), (SQ - 300, SQ)):
+        ref = oracle.qk_norm_rope_emulate(np.ascontiguousarray(q[:, s0:s1]), w, cos[s0:s1], sin[s0:s1], ROT, EPS)
+        ids = np.arange(s0 * H, s1 * H, dtype=np.int64)
+        got = _rows_back(dq_out, ids)
+        np.testing.assert_array_equal(got, ref.reshape(-1, D), err_msg=f"tokens {s0}..{s1}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kern", ["1", "4"], ids=["one_tile", "two_ctas"])
+def test_attention_past_2_to_the_31_elements(h3, big_inputs, monkeypatch, kern):
+    import torch
+    monkeypatch.setenv("H3ATTN_ATTN_KERNEL", kern)
+    q, k, v = big_inputs
+    dq, dk, dv = to_dev(q), to_dev(k), to_dev(v)
+    do = torch.full_like(dq, float("nan"))
+    scale = 1.0 / np.sqrt(D)
+    h3.h3attn_prefill(dq, dk, dv, do, scale)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    assert_convex_bound(dv, do, 1, "past 2^31 elements")
+    extra = (LINE - 1, LINE, LINE + 1, SQ - 129, SQ - 128, SQ - 2)
+    ids = sample_rows(B, SQ, H, 16, seed=3, extra_rows=extra)
+    ref = oracle.attention_f64(q, k, v, scale, row_ids=ids)
+    check_close(_rows_back(do, ids), ref, f"cross past 2^31 elements, kernel {kern}")
