@@ -1,9 +1,9 @@
 """Tensors past 2^31 elements (byte offsets past 2^32): the norm/RoPE kernel
 and the attention kernels the library picks for head dim 128 (one query tile
 per CTA; two CTAs per SM), on a cross-attention shape whose query has
-2^31 + 4.2 M elements (4.3 GB per tensor), compared with the oracle on sampled
-rows on both sides of the 2^31-element line.  Only the sampled rows come back
-to the host."""
+2^31 + 4.2 M elements (4.3 GB per tensor), and the RMSNorm -> AdaLN kernel on
+hidden rows of the same size, compared with the oracle on rows on both sides
+of the 2^31-element line.  Only the compared rows come back to the host."""
 import numpy as np
 import pytest
 
@@ -68,3 +68,30 @@ def test_attention_past_2_to_the_31_elements(h3, big_inputs, monkeypatch, kern):
     ids = sample_rows(B, SQ, H, 16, seed=3, extra_rows=extra)
     ref = oracle.attention_f64(q, k, v, scale, row_ids=ids)
     check_close(_rows_back(do, ids), ref, f"cross past 2^31 elements, kernel {kern}")
+
+
+@pytest.mark.gpu
+def test_rmsnorm_modulate_past_2_to_the_31_elements(h3):
+    """Hidden rows of 2^31 + 3.1 M elements (700 k rows of 3072 channels), bit-exact
+    on row ranges at the start, across the 2^31-element line and at the end."""
+    import torch
+    C, N = 3072, 21
+    T = (1 << 31) // C + 1024
+    inp = gen.make_modulate_inputs(T, C, N, seed=23)
+    assert inp.x.size > (1 << 31)
+
+    def dev2(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+    x = dev2(inp.x)
+    y = torch.empty_like(x)
+    h3.h3attn_rmsnorm_modulate(x, y, to_dev_f32(inp.w), dev2(inp.scale), dev2(inp.shift),
+                               torch.from_numpy(inp.idx).cuda(), 1e-6)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    line = (1 << 31) // C
+    for t0, t1 in ((0, 64), (line - 50, line + 50), (T - 200, T)):
+        ref = oracle.rmsnorm_modulate_emulate(np.ascontiguousarray(inp.x[t0:t1]), inp.w, inp.scale, inp.shift,
+                                              np.ascontiguousarray(inp.idx[t0:t1]), 1e-6)
+        got = y[t0:t1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        np.testing.assert_array_equal(got, ref, err_msg=f"rows {t0}..{t1}")
