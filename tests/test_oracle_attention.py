@@ -1,5 +1,7 @@
 """Pins of the oracle's dense prefill attention.
 
+Brute force: the definition written out on tiny inputs in long double,
+materialising each score matrix (separate code from the oracle's row loop).
 Against a library routine: torch's ``scaled_dot_product_attention`` in
 float64 on the CPU, with GQA expressed as K/V heads repeated, and the boolean
 [Q, K] mask (True = attend) that FastVideo PR #1799 ("Add opt-in FlashInfer
@@ -77,6 +79,42 @@ CASES = [
     ("bits", 2, 29, 45, 2, 2, 16, False, None, None, 0.6),
     ("bits_and_padding_causal", 2, 31, 31, 2, 1, 32, False, [17, 30], [0, 1], 0.7),
 ]
+
+
+def _brute_longdouble(q, k, v, scale, mask):
+    """The definition written out on tiny inputs, separate from the oracle's
+    code: per (sample, head) the whole score matrix in long double, then per
+    row the softmax over the allowed keys and the weighted sum of their value
+    rows; a row with no allowed key is 0."""
+    B, Sq, Hq, D = q.shape
+    Hkv = k.shape[2]
+    qf, kf, vf = (_bf(x).astype(np.longdouble) for x in (q, k, v))
+    out = np.zeros((B, Sq, Hq, D), np.longdouble)
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // (Hq // Hkv)
+            scores = (qf[b, :, h, :] @ kf[b, :, kvh, :].T) * np.longdouble(scale)
+            for i in range(Sq):
+                allowed = mask[b, i]
+                if not allowed.any():
+                    continue
+                s = scores[i, allowed]
+                p = np.exp(s - s.max())
+                out[b, i, h] = (p[:, None] * vf[b, allowed, kvh, :]).sum(axis=0) / p.sum()
+    return out
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_matches_long_double_brute_force(case):
+    name, B, Sq, Sk, Hq, Hkv, D, causal, kv_len, causal_b, dens = case
+    q, k, v = _rand(B, Sq, Sk, Hq, Hkv, D, seed=zlib.crc32(name.encode()) % 997 + 1)
+    kv_len = None if kv_len is None else np.array(kv_len, np.int32)
+    causal_b = None if causal_b is None else np.array(causal_b, np.uint8)
+    bits = None if dens is None else gen.bernoulli_bits(B, Sq, Sk, 5, gen.STREAM_BITS, dens)
+    scale = 1.0 / np.sqrt(D)
+    o = oracle.attention_f64(q, k, v, scale, causal, kv_len, None, causal_b, bits)
+    ref = _brute_longdouble(q, k, v, scale, _mask_matrix(B, Sq, Sk, causal, kv_len, None, causal_b, bits))
+    np.testing.assert_allclose(o, ref.astype(np.float64), rtol=1e-12, atol=1e-13)
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
