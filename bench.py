@@ -417,8 +417,9 @@ def _time_rmsnorm_modulate(h3, gen, torch, stream, peaks, steps=20, warmup=3):
     nbytes = 2.0 * mw.T * mw.C * 2 + 2.0 * mw.frames * mw.C * 2 + mw.C * 4 + mw.T * 4
     gbs = nbytes / (ms * 1e-3) / 1e9
     # the launcher's shape: 16 compute warps per CTA while an 18-row ring fits one SM, else 8
-    w_mod = 16 if 18 * (2 * mw.C + 16) <= 233472 - 1040 else 8
-    return {"kernel": f"rmsnorm_modulate_kernel<{w_mod}>", "workload": f"{mw.name}: T={mw.T} C={mw.C} N={mw.frames}",
+    w_mod, staged = _mod_shape(mw.C, with_weight=True)
+    return {"kernel": f"rmsnorm_modulate_kernel<{w_mod}>" + (" (weight staged in shared memory)" if staged else ""),
+            "workload": f"{mw.name}: T={mw.T} C={mw.C} N={mw.frames}",
             "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": int(nbytes),
             "ms_per_launch": round(ms, 4), "launches": steps + warmup,
@@ -498,6 +499,25 @@ def _attn_kernel_name(wl):
     if sel == "2":
         return {64: "attn_fwd_kernel<64,2,8,1>", 128: "attn_fwd_kernel<128,2,4,1>"}[wl.D]
     return {64: "attn_fwd_kernel<64,1,4,2>", 128: "attn_fwd_kernel<128,1,2,2>"}[wl.D]
+
+
+def _mod_shape(C, with_weight):
+    """(compute warps per CTA, weight staged) that the library's AdaLN launcher
+    picks for C channels: the first (warps, CTAs per SM) shape whose ring holds
+    warps + 2 rows of 2C + 16 bytes, with the weight (4C bytes) staged when that
+    keeps at least 3/4 of the compute warps per SM.  Used for labels only."""
+    shapes = [(16, 2), (14, 2), (8, 4), (8, 3), (16, 1), (8, 2), (8, 1)]
+
+    def pick(extra):
+        for w, ctas in shapes:
+            if (233472 // ctas - 1040 - extra) // (2 * C + 16) >= w + 2:
+                return w, ctas
+        return None
+    plain = pick(0)
+    staged = pick(4 * C) if with_weight else None
+    if staged is not None and (plain is None or 4 * staged[0] * staged[1] >= 3 * plain[0] * plain[1]):
+        return staged[0], True
+    return (plain[0] if plain else 0), False
 
 
 def _profiled_traffic():

@@ -42,3 +42,14 @@ def test_window_pairs_match_oracle_count():
     for S, L, geo in ((104448, 104448, (1536, 1, 5, 1)), (2000, 1500, (100, 1, 5, 1)), (777, 777, (7, 0, 3, 2)),
                       (500, 500, (10, 60, 2, 1))):
         assert bench._window_pairs(S, L, *geo) == oracle.window_allowed_pairs(S, L, *geo)
+
+
+def test_modulate_shape_label_follows_the_launcher_rule():
+    import bench
+    # C 3072 with a weight: 14 compute warps x 2 CTAs with the weight staged
+    # (28 >= 3/4 of the 32 warps without it); without a weight, 16 x 2
+    assert bench._mod_shape(3072, True) == (14, True)
+    assert bench._mod_shape(3072, False) == (16, False)
+    # C 6144: staging would leave 8 of 16 warps, so the weight is read through L1
+    assert bench._mod_shape(6144, True) == (16, False)
+    assert bench._mod_shape(8192, True) == (8, True)

@@ -57,17 +57,21 @@ def test_bit_exact_edge_shapes(h3, T, C, N):
 
 
 # Every ring shape the launcher picks, with many rows per CTA so that each
-# compute warp goes round its CTA's ring several times (C 1536: 16 warps, 37
-# stages, 2 CTAs per SM; 4096 / 5120: 16 warps, 1 CTA; 8192: 8 warps, 14
-# stages, 1 CTA); every stage is refilled at least twice.  A ring with fewer
-# stages than compute warps would hand a warp a stale row here.
+# compute warp goes round its CTA's ring several times (C 1536: 16 warps, 35
+# stages, 2 CTAs per SM; 3072: 14 warps, 16 stages, 2 CTAs, weight staged;
+# 3456: 14 warps, 16 stages, 2 CTAs, weight through L1; 4096 / 5120: 16 warps,
+# 1 CTA; 8192: 8 warps, 12 stages, 1 CTA); every stage is refilled at least
+# twice.  A ring with fewer stages than compute warps would hand a warp a
+# stale row here.  Without the weight the same sizes take the other shapes.
 @pytest.mark.gpu
-@pytest.mark.parametrize("T,C,N", [(24000, 1536, 4), (9000, 4096, 3), (7000, 5120, 3), (4500, 8192, 2)])
-def test_bit_exact_rows_lap_the_ring(h3, T, C, N):
+@pytest.mark.parametrize("with_w", [True, False], ids=["weight", "no_weight"])
+@pytest.mark.parametrize("T,C,N", [(24000, 1536, 4), (20000, 3072, 4), (11000, 3456, 3), (9000, 4096, 3),
+                                   (7000, 5120, 3), (6000, 6144, 3), (4500, 8192, 2)])
+def test_bit_exact_rows_lap_the_ring(h3, T, C, N, with_w):
     inp = gen.make_modulate_inputs(T, C, N, seed=T ^ C)
-    got = _run(h3, inp)
+    got = _run(h3, inp, with_w=with_w)
     assert h3.h3attn_check_device_status() == 0
-    _assert_bits_equal(got, _expect(inp), f"T={T} C={C}")
+    _assert_bits_equal(got, _expect(inp, with_w=with_w), f"T={T} C={C} weight={with_w}")
 
 
 @pytest.mark.gpu

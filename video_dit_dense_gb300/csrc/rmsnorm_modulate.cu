@@ -52,7 +52,9 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 // one-row shared-memory stages: one producer warp bulk-copies rows ahead as
 // stages free up, and compute warp w takes rows w, w + W, ... of the CTA's
 // range.  The ring keeps up to NS - W rows of HBM reads in flight per CTA
-// beyond the rows the compute warps hold.
+// beyond the rows the compute warps hold.  With stage_w the float32 norm
+// weight is copied once into shared memory after the ring, so the per-row
+// loads through L1 are only the scale / shift rows.
 //
 // Ring invariant NS >= W (the launcher guarantees it).  When warp w waits for
 // row i (fill i / NS of stage i % NS), the stage's previous fill holds row
@@ -62,7 +64,7 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 // instead and take a stale row.
 template <int W>
 __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
-    rmsnorm_modulate_kernel(const __grid_constant__ ModArgs a, int NS) {
+    rmsnorm_modulate_kernel(const __grid_constant__ ModArgs a, int NS, int stage_w) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -73,6 +75,8 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
   auto bar_full = [&](int st) { return bars + 8u * st; };
   auto bar_empty = [&](int st) { return bars + 8u * (NS + st); };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + NS * row_bytes + 16 * NS);
+  // staged norm weight: after the barriers and the abort word (16-byte aligned: row_bytes and 16 NS are)
+  float* wsm = reinterpret_cast<float*>(smem + NS * row_bytes + 16 * NS + 16);
   WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
   if (threadIdx.x == 0) {
     for (int st = 0; st < NS; ++st) {
@@ -81,6 +85,10 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
     }
     *abort_flag = 0u;
     fence_barrier_init();
+  }
+  if (stage_w) {
+    for (int i = threadIdx.x; i < (C >> 2); i += blockDim.x)
+      reinterpret_cast<float4*>(wsm)[i] = __ldg(reinterpret_cast<const float4*>(a.w) + i);
   }
   __syncthreads();
   // rows of this CTA: a contiguous range t_i = r0 + i, i < n (neighbouring
@@ -149,8 +157,14 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
         const uint32_t h4[4] = {hv.x, hv.y, hv.z, hv.w};
         float wv[8];
         if (a.w) {
-          const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.w + 8 * g));
-          const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.w + 8 * g + 4));
+          float4 w0, w1;
+          if (stage_w) {
+            w0 = reinterpret_cast<const float4*>(wsm)[2 * g];
+            w1 = reinterpret_cast<const float4*>(wsm)[2 * g + 1];
+          } else {
+            w0 = __ldg(reinterpret_cast<const float4*>(a.w + 8 * g));
+            w1 = __ldg(reinterpret_cast<const float4*>(a.w + 8 * g + 4));
+          }
           wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
           wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
         }
@@ -174,7 +188,7 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
 }
 
 template <int W>
-cudaError_t launch_with(const ModArgs& a, int ctas_per_sm, int NS, size_t smem, cudaStream_t stream) {
+cudaError_t launch_with(const ModArgs& a, int ctas_per_sm, int NS, int stage_w, size_t smem, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -190,7 +204,7 @@ cudaError_t launch_with(const ModArgs& a, int ctas_per_sm, int NS, size_t smem, 
   if (e != cudaSuccess) return e;
   int64_t blocks = static_cast<int64_t>(sms) * ctas_per_sm;
   if (blocks > a.T) blocks = a.T;
-  rmsnorm_modulate_kernel<W><<<static_cast<unsigned>(blocks), (W + 1) * 32, smem, stream>>>(a, NS);
+  rmsnorm_modulate_kernel<W><<<static_cast<unsigned>(blocks), (W + 1) * 32, smem, stream>>>(a, NS, stage_w);
   return cudaGetLastError();
 }
 
@@ -200,25 +214,43 @@ cudaError_t launch_with(const ModArgs& a, int ctas_per_sm, int NS, size_t smem, 
 // latency-bound per warp: 16 compute warps per SM reached 4.44 TB/s, 32
 // reached 5.3 TB/s on T 32760 x C 3072), each ring holding at least W + 2
 // rows (the invariant NS >= W plus two rows of read-ahead), then the deepest
-// ring that fits beside the other CTAs of the SM.
+// ring that fits beside the other CTAs of the SM.  The weight is staged in
+// shared memory when the shape that leaves room for it keeps at least 3/4 of
+// the compute warps of the shape without it (C 3072: 28 warps with the staged
+// weight measured 2.2 % faster than 32 loading it through L1).
 cudaError_t launch_rmsnorm_modulate(const ModArgs& a, cudaStream_t stream) {
   constexpr int64_t kSmemPerSm = 233472;  // 228 KiB, of which 1 KiB per CTA is reserved
   constexpr int64_t kMaxNS = 48;
   const int64_t stage = static_cast<int64_t>(a.C) * 2 + 16;  // one row + its two barriers
   struct Shape {
     int W, ctas;
+    int64_t NS;
   };
-  const Shape shapes[] = {{16, 2}, {8, 4}, {8, 3}, {16, 1}, {8, 2}, {8, 1}};
-  for (const Shape& sh : shapes) {
-    const int64_t per_cta = kSmemPerSm / sh.ctas - 1024 - 16;  // ring + abort word
-    int64_t NS = per_cta / stage;
-    if (NS < sh.W + 2) continue;
-    if (NS > kMaxNS) NS = kMaxNS;
-    const size_t smem = static_cast<size_t>(NS * stage + 16);
-    if (sh.W == 16) return launch_with<16>(a, sh.ctas, static_cast<int>(NS), smem, stream);
-    return launch_with<8>(a, sh.ctas, static_cast<int>(NS), smem, stream);
-  }
-  return cudaErrorInvalidValue;  // a row larger than the shared memory of an SM
+  const Shape shapes[] = {{16, 2, 0}, {14, 2, 0}, {8, 4, 0}, {8, 3, 0}, {16, 1, 0}, {8, 2, 0}, {8, 1, 0}};
+  // first shape of the table whose ring fits beside `extra` bytes per CTA
+  auto pick = [&](int64_t extra, Shape* out) {
+    for (const Shape& sh : shapes) {
+      const int64_t per_cta = kSmemPerSm / sh.ctas - 1024 - 16 - extra;  // ring (+ abort word, extra)
+      int64_t NS = per_cta / stage;
+      if (NS < sh.W + 2) continue;
+      *out = {sh.W, sh.ctas, NS > kMaxNS ? kMaxNS : NS};
+      return true;
+    }
+    return false;
+  };
+  const int64_t wbytes = static_cast<int64_t>(a.C) * 4;
+  Shape plain{}, staged{};
+  const bool has_plain = pick(0, &plain);
+  const bool has_staged = a.w != nullptr && pick(wbytes, &staged);
+  const bool use_staged =
+      has_staged && (!has_plain || 4 * staged.W * staged.ctas >= 3 * plain.W * plain.ctas);
+  if (!use_staged && !has_plain) return cudaErrorInvalidValue;  // a row larger than an SM's shared memory
+  const Shape sh = use_staged ? staged : plain;
+  const size_t smem = static_cast<size_t>(sh.NS * stage + 16 + (use_staged ? wbytes : 0));
+  const int NS = static_cast<int>(sh.NS), sw = use_staged ? 1 : 0;
+  if (sh.W == 16) return launch_with<16>(a, sh.ctas, NS, sw, smem, stream);
+  if (sh.W == 14) return launch_with<14>(a, sh.ctas, NS, sw, smem, stream);
+  return launch_with<8>(a, sh.ctas, NS, sw, smem, stream);
 }
 
 }  // namespace h3
