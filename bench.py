@@ -416,7 +416,7 @@ def _time_rmsnorm_modulate(h3, gen, torch, stream, peaks, steps=20, warmup=3):
     ms = e0.elapsed_time(e1) / steps
     nbytes = 2.0 * mw.T * mw.C * 2 + 2.0 * mw.frames * mw.C * 2 + mw.C * 4 + mw.T * 4
     gbs = nbytes / (ms * 1e-3) / 1e9
-    # the launcher's shape: 16 compute warps per CTA while an 18-row ring fits one SM, else 8
+    # the shape the library's launcher picks (label only)
     w_mod, staged = _mod_shape(mw.C, with_weight=True)
     return {"kernel": f"rmsnorm_modulate_kernel<{w_mod}>" + (" (weight staged in shared memory)" if staged else ""),
             "workload": f"{mw.name}: T={mw.T} C={mw.C} N={mw.frames}",
