@@ -61,8 +61,9 @@ def test_bit_exact_edge_shapes(h3, T, C, N):
 # stages, 2 CTAs per SM; 3072: 14 warps, 16 stages, 2 CTAs, weight staged;
 # 3456: 14 warps, 16 stages, 2 CTAs, weight through L1; 4096 / 5120: 16 warps,
 # 1 CTA; 8192: 8 warps, 12 stages, 1 CTA); every stage is refilled at least
-# twice.  A ring with fewer stages than compute warps would hand a warp a
-# stale row here.  Without the weight the same sizes take the other shapes.
+# twice, so a warp that took a stale fill of its stage (phase aliasing) would
+# show here as a wrong row.  Without the weight the same sizes take the other
+# shapes.
 @pytest.mark.gpu
 @pytest.mark.parametrize("with_w", [True, False], ids=["weight", "no_weight"])
 @pytest.mark.parametrize("T,C,N", [(24000, 1536, 4), (20000, 3072, 4), (11000, 3456, 3), (9000, 4096, 3),

@@ -48,6 +48,30 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Count of rows the producer has issued, published with release semantics
+// (shared memory, CTA scope), and the bounded wait on it.
+__device__ __forceinline__ void st_release_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool issued_wait(uint32_t addr, uint32_t need, const WaitCtl& ctl) {
+  if (ld_acquire_u32(addr) >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_u32(addr) < need) {
+    if (*ctl.abort_flag) return false;
+    if (globaltimer_ns() - t0 > ctl.limit_ns) {
+      *ctl.abort_flag = 1u;
+      atomicExch(ctl.status, ctl.timeout_code);
+      return false;
+    }
+  }
+  return true;
+}
+
 // A persistent CTA streams a contiguous range of rows through a ring of NS
 // one-row shared-memory stages: one producer warp bulk-copies rows ahead as
 // stages free up, and compute warp w takes rows w, w + W, ... of the CTA's
@@ -56,12 +80,15 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 // weight is copied once into shared memory after the ring, so the per-row
 // loads through L1 are only the scale / shift rows.
 //
-// Ring invariant NS >= W (the launcher guarantees it).  When warp w waits for
-// row i (fill i / NS of stage i % NS), the stage's previous fill holds row
-// i - NS <= i - W; rows land in order and warp w has already consumed row
-// i - W, so that fill has landed and the phase parity names fill i / NS
-// unambiguously.  With NS < W a warp could find fill i / NS - 2 complete
-// instead and take a stale row.
+// Phase aliasing.  Warp w waits for row i as fill f = i / NS of stage
+// i % NS.  A parity wait passes when fill f has landed, but also when only
+// fills up to f - 2 have (fill f - 1, row i - NS, still in flight): row
+// i - NS belongs to another warp unless NS == W, and bulk copies complete in
+// any order, so a warp could take the stale row i - 2 NS.  The producer
+// therefore publishes how many rows it has issued, and warp w first waits
+// for row i to be issued: that happens only after row i - NS was consumed,
+// hence landed, so the parity then names fill f alone.  This holds for any
+// NS; the launcher's NS >= W + 2 is for read-ahead.
 template <int W>
 __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
     rmsnorm_modulate_kernel(const __grid_constant__ ModArgs a, int NS, int stage_w) {
@@ -75,6 +102,7 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
   auto bar_full = [&](int st) { return bars + 8u * st; };
   auto bar_empty = [&](int st) { return bars + 8u * (NS + st); };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + NS * row_bytes + 16 * NS);
+  const uint32_t issued = smem_u32(smem + NS * row_bytes + 16 * NS + 4);  // rows issued by the producer
   // staged norm weight: after the barriers and the abort word (16-byte aligned: row_bytes and 16 NS are)
   float* wsm = reinterpret_cast<float*>(smem + NS * row_bytes + 16 * NS + 16);
   WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
@@ -84,6 +112,7 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
       mbar_init(bar_empty(st), 1);
     }
     *abort_flag = 0u;
+    *reinterpret_cast<volatile uint32_t*>(smem + NS * row_bytes + 16 * NS + 4) = 0u;
     fence_barrier_init();
   }
   if (stage_w) {
@@ -106,6 +135,7 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
         if (!mbar_wait(bar_empty(st), static_cast<uint32_t>((i / NS) & 1) ^ 1u, ctl)) break;
         mbar_arrive_expect_tx(bar_full(st), row_bytes);
         bulk_load(sbase + st * row_bytes, a.x + (r0 + i) * C, row_bytes, bar_full(st));
+        st_release_u32(issued, static_cast<uint32_t>(i + 1));
       }
       // every issued copy has landed before the CTA retires
       for (int64_t k = i > NS ? i - NS : 0; k < i; ++k) {
@@ -121,7 +151,8 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
   const uint32_t one2 = 0x3F803F80u;  // bf16x2 (1, 1)
   for (int64_t i = warp; i < n; i += W) {
     const int st = static_cast<int>(i % NS);
-    const bool ok = mbar_wait(bar_full(st), static_cast<uint32_t>((i / NS) & 1), ctl);
+    const bool ok = issued_wait(issued, static_cast<uint32_t>(i + 1), ctl) &&
+                    mbar_wait(bar_full(st), static_cast<uint32_t>((i / NS) & 1), ctl);
     if (!__all_sync(0xFFFFFFFFu, ok)) break;
     const int64_t t = r0 + i;
     const uint4* xs = reinterpret_cast<const uint4*>(smem + st * row_bytes);
@@ -213,8 +244,8 @@ cudaError_t launch_with(const ModArgs& a, int ctas_per_sm, int NS, int stage_w, 
 // Shape: as many compute warps per SM as the rings allow (the kernel is
 // latency-bound per warp: 16 compute warps per SM reached 4.44 TB/s, 32
 // reached 5.3 TB/s on T 32760 x C 3072), each ring holding at least W + 2
-// rows (the invariant NS >= W plus two rows of read-ahead), then the deepest
-// ring that fits beside the other CTAs of the SM.  The weight is staged in
+// rows (one per compute warp plus two of read-ahead), then the deepest ring
+// that fits beside the other CTAs of the SM.  The weight is staged in
 // shared memory when the shape that leaves room for it keeps at least 3/4 of
 // the compute warps of the shape without it (C 3072: 28 warps with the staged
 // weight measured 2.2 % faster than 32 loading it through L1).
@@ -230,7 +261,7 @@ cudaError_t launch_rmsnorm_modulate(const ModArgs& a, cudaStream_t stream) {
   // first shape of the table whose ring fits beside `extra` bytes per CTA
   auto pick = [&](int64_t extra, Shape* out) {
     for (const Shape& sh : shapes) {
-      const int64_t per_cta = kSmemPerSm / sh.ctas - 1024 - 16 - extra;  // ring (+ abort word, extra)
+      const int64_t per_cta = kSmemPerSm / sh.ctas - 1024 - 16 - extra;  // ring (+ abort word and issued count, extra)
       int64_t NS = per_cta / stage;
       if (NS < sh.W + 2) continue;
       *out = {sh.W, sh.ctas, NS > kMaxNS ? kMaxNS : NS};
