@@ -1,0 +1,232 @@
+"""A model of the one-query-tile attention pipeline's synchronisation (host
+logic, no GPU), as the persistent kernel runs it over a stream of units (the
+single-CTA-per-unit kernel is the one-unit case).
+
+Roles: a producer fills an NSTAGE ring in the order K0, K1, K2, then K_{J+3},
+V_J; two MMA-issuing threads take even / odd key tiles (thread p issues
+O += P_J V_J and then S_{J+3} = Q K_{J+3}^T into score buffer (J+1) mod 2);
+the softmax reads S_J, publishes P_J into a single P buffer once
+O += P_{J-1} V_{J-1} has completed, writes the next unit's Q once the current
+unit's last score tile is read, and reads O at each unit's end.  mbarrier
+waits are parity waits (pass iff completed phases % 2 != parity); each MMA
+thread's tensor-core operations complete in its own issue order; bulk copies
+complete in any order.  Checked in every interleaving: every product reads
+the stage, score buffer, P and Q it was meant to, the first P V of a unit
+overwrites O only after the previous epilogue read it, nothing deadlocks.
+
+The Q hand-off is a count of written query rows that an MMA thread waits on
+before the first Q K^T of a unit.  The model also runs the hand-off it
+replaced, a parity barrier, and finds the failure it had: an MMA thread that
+skips a one-tile unit can no longer tell unit k's Q from unit k - 2's."""
+import random
+
+import pytest
+
+
+class Bar:
+    """An mbarrier with an arrival count, counting completed phases."""
+
+    def __init__(self, count=1):
+        self.count, self.pending, self.done = count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        if self.pending == 0:
+            self.done += 1
+            self.pending = self.count
+
+    def ok(self, parity):
+        return (self.done & 1) != parity
+
+
+def run_pipe(units, seed, nstage, q_handoff="count"):
+    """One random interleaving over units of the given key-tile counts (0 =
+    a unit with no key tile, which only writes zero rows and joins no stream).
+    Returns the list of protocol violations (empty = clean)."""
+    rng = random.Random(seed)
+    tiles = []   # (unit seq, tile index in unit) of each stream tile J
+    seq = 0
+    for n in units:
+        if n > 0:
+            tiles.extend((seq, j) for j in range(n))
+            seq += 1
+    n_units = seq
+    N = len(tiles)
+    kv_full = [Bar() for _ in range(nstage)]
+    kv_empty = [Bar() for _ in range(nstage)]
+    s_full, s_read = [Bar(), Bar()], [Bar(), Bar()]
+    p_ready, pv_done = [Bar(), Bar()], [Bar(), Bar()]
+    q_full = Bar()
+    st = {"q_ready": 0, "Q": None, "S": [None, None], "P": None, "O": None, "O_read": True,
+          "stage": [None] * nstage}
+    queues = {0: [], 1: []}   # tensor-core operations of each MMA thread, in issue order
+    copies = []               # bulk copies in flight: (stage, contents)
+    errors = []
+
+    def load_of_v(J):
+        return min(J + 4, N) + J
+
+    def load_of_k(J):
+        return J if J < 3 else 2 * J - 3
+
+    def buf_parity(J):        # tile J is use J // 2 of buffer J % 2
+        return (J >> 1) & 1
+
+    def producer():
+        order = [("K", j) for j in range(min(3, N))]
+        for J in range(N):
+            if J + 3 < N:
+                order.append(("K", J + 3))
+            order.append(("V", J))
+        for ld, what in enumerate(order):
+            sidx, ph = ld % nstage, (ld // nstage) & 1
+            yield lambda sidx=sidx, ph=ph: kv_empty[sidx].ok(ph ^ 1)
+            copies.append((sidx, what))
+
+    def mma(p):
+        if N <= p:
+            return
+        q_seq = [-1]
+
+        def issue_qk(J):
+            useq = tiles[J][0]
+            if useq != q_seq[0]:
+                if q_handoff == "count":
+                    yield lambda: st["q_ready"] >= useq + 1
+                else:
+                    yield lambda: q_full.ok(useq & 1)
+                q_seq[0] = useq
+            ld = load_of_k(J)
+            sidx, ph = ld % nstage, (ld // nstage) & 1
+            yield lambda: kv_full[sidx].ok(ph)
+            if J >= 2:
+                yield lambda: s_read[J & 1].ok(buf_parity(J - 2))
+            queues[p].extend([("qk", J, sidx), ("commit", s_full[J & 1]), ("commit", kv_empty[sidx])])
+
+        yield from issue_qk(p)
+        if p == 1 and N > 2:
+            yield from issue_qk(2)
+        for J in range(p, N, 2):
+            ld = load_of_v(J)
+            sidx, ph = ld % nstage, (ld // nstage) & 1
+            yield lambda: kv_full[sidx].ok(ph)
+            yield lambda: p_ready[p].ok(buf_parity(J))
+            queues[p].extend([("pv", J, sidx), ("commit", pv_done[p]), ("commit", kv_empty[sidx])])
+            if J + 3 < N:
+                yield from issue_qk(J + 3)
+
+    def write_q(useq):
+        st["Q"] = useq
+        if q_handoff == "count":
+            st["q_ready"] += 1
+        else:
+            q_full.arrive()
+
+    def softmax():
+        J = 0
+        if N:
+            write_q(0)
+        useq = 0
+        for n in units:
+            if n == 0:
+                continue
+            for j in range(n):
+                yield lambda: s_full[J & 1].ok(buf_parity(J))
+                if st["S"][J & 1] != J:
+                    errors.append(f"softmax reads score buffer {J & 1} holding tile {st['S'][J & 1]} for tile {J}")
+                if j == n - 1 and useq + 1 < n_units:
+                    write_q(useq + 1)
+                s_read[J & 1].arrive()
+                if J > 0:
+                    yield lambda: pv_done[(J - 1) & 1].ok(buf_parity(J - 1))
+                st["P"] = J
+                p_ready[J & 1].arrive()
+                J += 1
+            yield lambda: pv_done[(J - 1) & 1].ok(buf_parity(J - 1))
+            if st["O"] != (useq, n):
+                errors.append(f"epilogue of unit {useq} reads O {st['O']}")
+            st["O_read"] = True
+            useq += 1
+
+    def execute(p):
+        op = queues[p].pop(0)
+        if op[0] == "commit":
+            op[1].arrive()
+        elif op[0] == "qk":
+            J, sidx = op[1], op[2]
+            if st["stage"][sidx] != ("K", J):
+                errors.append(f"Q K^T of tile {J} reads stage {sidx} holding {st['stage'][sidx]}")
+            if st["Q"] != tiles[J][0]:
+                errors.append(f"Q K^T of tile {J} (unit {tiles[J][0]}) reads the Q of unit {st['Q']}")
+            st["S"][J & 1] = J
+        else:
+            J, sidx = op[1], op[2]
+            if st["stage"][sidx] != ("V", J):
+                errors.append(f"P V of tile {J} reads stage {sidx} holding {st['stage'][sidx]}")
+            if st["P"] != J:
+                errors.append(f"P V of tile {J} reads P of tile {st['P']}")
+            useq, j = tiles[J]
+            if j == 0:
+                if not st["O_read"]:
+                    errors.append(f"P V of tile {J} overwrites O before the epilogue read it")
+                st["O"], st["O_read"] = (useq, 1), False
+            else:
+                if st["O"] != (useq, j):
+                    errors.append(f"P V of tile {J} accumulates onto O {st['O']}")
+                st["O"] = (useq, j + 1)
+
+    roles = {"producer": producer(), "mma0": mma(0), "mma1": mma(1), "softmax": softmax()}
+    waits = {}
+    for name in list(roles):
+        try:
+            waits[name] = next(roles[name])
+        except StopIteration:
+            del roles[name]
+    while roles or queues[0] or queues[1] or copies:
+        moves = [("role", r) for r in roles if waits[r]()]
+        moves += [("tensor", p) for p in (0, 1) if queues[p]]
+        moves += [("copy", i) for i in range(len(copies))]
+        if not moves:
+            return [f"deadlock: {sorted(roles)} waiting"]
+        kind, x = rng.choice(moves)
+        if kind == "role":
+            try:
+                waits[x] = roles[x].send(None)
+            except StopIteration:
+                del roles[x]
+        elif kind == "tensor":
+            execute(x)
+        else:
+            sidx, what = copies.pop(x)
+            st["stage"][sidx] = what
+            kv_full[sidx].arrive()
+        if errors:
+            return errors
+    return errors
+
+
+def _random_units(rng):
+    return [rng.choice([0, 1, 1, 2, 3, 5]) for _ in range(rng.randint(1, 7))]
+
+
+@pytest.mark.parametrize("nstage", [4, 7, 12])
+def test_count_handoff_pipeline_is_clean(nstage):
+    rng = random.Random(nstage)
+    for trial in range(400):
+        units = _random_units(rng)
+        assert run_pipe(units, trial, nstage) == [], f"units {units}, seed {trial}"
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 40])
+def test_single_unit_pipeline_is_clean(n):
+    # the default kernel: one unit per CTA
+    for trial in range(100):
+        assert run_pipe([n], trial, 7) == []
+
+
+def test_parity_handoff_of_q_can_alias():
+    rng = random.Random(7)
+    failures = 0
+    for trial in range(1500):
+        failures += bool(run_pipe(_random_units(rng), trial, 7, q_handoff="parity"))
+    assert failures > 0
