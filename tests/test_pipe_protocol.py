@@ -17,7 +17,12 @@ overwrites O only after the previous epilogue read it, nothing deadlocks.
 The Q hand-off is a count of written query rows that an MMA thread waits on
 before the first Q K^T of a unit.  The model also runs the hand-off it
 replaced, a parity barrier, and finds the failure it had: an MMA thread that
-skips a one-tile unit can no longer tell unit k's Q from unit k - 2's."""
+skips a one-tile unit can no longer tell unit k's Q from unit k - 2's.
+
+The padding warp (one unit per CTA) zeroes the V rows past kv_len of the key
+tile that straddles it: it waits for the producer's flag that the tile's V
+load is issued, then for the stage's phase, and the tile's P V waits for it.
+Without the flag the phase wait could pass on an older fill of the stage."""
 import random
 
 import pytest
@@ -39,10 +44,13 @@ class Bar:
         return (self.done & 1) != parity
 
 
-def run_pipe(units, seed, nstage, q_handoff="count"):
+def run_pipe(units, seed, nstage, q_handoff="count", pad_tile=None, pad_flag=True):
     """One random interleaving over units of the given key-tile counts (0 =
     a unit with no key tile, which only writes zero rows and joins no stream).
-    Returns the list of protocol violations (empty = clean)."""
+    pad_tile: (one unit only) the key tile that straddles kv_len, whose V rows
+    past kv_len a padding warp zeroes before that tile's P V; it first waits
+    for the producer's flag that the tile's V load is issued (pad_flag), then
+    for the stage's phase.  Returns the list of protocol violations."""
     rng = random.Random(seed)
     tiles = []   # (unit seq, tile index in unit) of each stream tile J
     seq = 0
@@ -57,8 +65,9 @@ def run_pipe(units, seed, nstage, q_handoff="count"):
     s_full, s_read = [Bar(), Bar()], [Bar(), Bar()]
     p_ready, pv_done = [Bar(), Bar()], [Bar(), Bar()]
     q_full = Bar()
+    v_clean = Bar()
     st = {"q_ready": 0, "Q": None, "S": [None, None], "P": None, "O": None, "O_read": True,
-          "stage": [None] * nstage}
+          "stage": [None] * nstage, "pad_issued": False, "zeroed": None}
     queues = {0: [], 1: []}   # tensor-core operations of each MMA thread, in issue order
     copies = []               # bulk copies in flight: (stage, contents)
     errors = []
@@ -82,6 +91,19 @@ def run_pipe(units, seed, nstage, q_handoff="count"):
             sidx, ph = ld % nstage, (ld // nstage) & 1
             yield lambda sidx=sidx, ph=ph: kv_empty[sidx].ok(ph ^ 1)
             copies.append((sidx, what))
+            if what == ("V", pad_tile):
+                st["pad_issued"] = True
+
+    def pad_warp():
+        ld = load_of_v(pad_tile)
+        sidx, ph = ld % nstage, (ld // nstage) & 1
+        if pad_flag:
+            yield lambda: st["pad_issued"]
+        yield lambda: kv_full[sidx].ok(ph)
+        if st["stage"][sidx] != ("V", pad_tile):
+            errors.append(f"padding warp zeroes stage {sidx} holding {st['stage'][sidx]}, not V of tile {pad_tile}")
+        st["zeroed"] = pad_tile
+        v_clean.arrive()
 
     def mma(p):
         if N <= p:
@@ -111,6 +133,8 @@ def run_pipe(units, seed, nstage, q_handoff="count"):
             sidx, ph = ld % nstage, (ld // nstage) & 1
             yield lambda: kv_full[sidx].ok(ph)
             yield lambda: p_ready[p].ok(buf_parity(J))
+            if J == pad_tile:
+                yield lambda: v_clean.ok(0)
             queues[p].extend([("pv", J, sidx), ("commit", pv_done[p]), ("commit", kv_empty[sidx])])
             if J + 3 < N:
                 yield from issue_qk(J + 3)
@@ -165,6 +189,8 @@ def run_pipe(units, seed, nstage, q_handoff="count"):
                 errors.append(f"P V of tile {J} reads stage {sidx} holding {st['stage'][sidx]}")
             if st["P"] != J:
                 errors.append(f"P V of tile {J} reads P of tile {st['P']}")
+            if J == pad_tile and st["zeroed"] != J:
+                errors.append(f"P V of tile {J} reads V before its padding rows were zeroed")
             useq, j = tiles[J]
             if j == 0:
                 if not st["O_read"]:
@@ -176,6 +202,9 @@ def run_pipe(units, seed, nstage, q_handoff="count"):
                 st["O"] = (useq, j + 1)
 
     roles = {"producer": producer(), "mma0": mma(0), "mma1": mma(1), "softmax": softmax()}
+    if pad_tile is not None:
+        assert len(units) == 1 and 0 <= pad_tile < units[0]
+        roles["pad"] = pad_warp()
     waits = {}
     for name in list(roles):
         try:
@@ -230,3 +259,18 @@ def test_parity_handoff_of_q_can_alias():
     for trial in range(1500):
         failures += bool(run_pipe(_random_units(rng), trial, 7, q_handoff="parity"))
     assert failures > 0
+
+
+@pytest.mark.parametrize("n", [1, 3, 9, 40])
+def test_padding_warp_zeroes_the_right_tile_before_its_product(n):
+    for trial in range(60):
+        for pad in sorted({0, n // 2, n - 1}):
+            assert run_pipe([n], trial, 7, pad_tile=pad) == [], f"n {n}, pad tile {pad}, seed {trial}"
+
+
+def test_padding_warp_without_the_issue_flag_can_take_an_older_fill():
+    # a phase wait counted from the kernel's start alone: the stage may pass
+    # on a fill two rounds older, or be empty, when the padding tile's V is a
+    # later fill of its stage
+    bad = sum(bool(run_pipe([40], trial, 7, pad_tile=20, pad_flag=False)) for trial in range(200))
+    assert bad > 0
