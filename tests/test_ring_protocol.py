@@ -83,3 +83,53 @@ def test_parity_alone_is_safe_only_with_in_order_landing_and_ns_at_least_w():
 def test_parity_alone_can_read_a_stale_row(W, NS, in_order):
     rng = random.Random(W * 1000 + NS)
     assert any(run_ring(3 * NS + 5, W, NS, rng, issued_count=False, in_order=in_order) > 0 for _ in range(3000))
+
+
+def run_broadcast_ring(n_chunks: int, W: int, NS: int, rng: random.Random) -> int:
+    """The norm/RoPE kernel's ring: every compute warp reads every chunk (its
+    own rows of it) in chunk order, the stage's "empty" barrier completes when
+    all W warps have arrived, and the waits are parity waits alone.  A warp
+    waiting for chunk c has itself consumed chunk c - NS of the same stage, so
+    that fill has landed whatever order the copies complete in.  Returns the
+    number of stale reads."""
+    full = [0] * NS
+    empty_arrivals = [0] * NS
+    data = [None] * NS
+    in_flight = []
+    issued = 0
+    next_chunk = [0] * W
+    stale = 0
+    while True:
+        moves = []
+        if issued < n_chunks and _parity_passed(empty_arrivals[issued % NS] // W, ((issued // NS) & 1) ^ 1):
+            moves.append(("produce", None))
+        if in_flight:
+            moves.append(("land", None))
+        for w in range(W):
+            c = next_chunk[w]
+            if c < n_chunks and _parity_passed(full[c % NS], (c // NS) & 1):
+                moves.append(("consume", w))
+        if not moves:
+            break
+        kind, w = rng.choice(moves)
+        if kind == "produce":
+            in_flight.append((issued % NS, issued))
+            issued += 1
+        elif kind == "land":
+            st, c = in_flight.pop(rng.randrange(len(in_flight)))
+            data[st] = c
+            full[st] += 1
+        else:
+            c = next_chunk[w]
+            stale += data[c % NS] != c
+            empty_arrivals[c % NS] += 1
+            next_chunk[w] = c + 1
+    assert all(c >= n_chunks for c in next_chunk), "deadlock"
+    return stale
+
+
+@pytest.mark.parametrize("W,NS", [(8, 2), (8, 3), (4, 3)])
+def test_broadcast_ring_of_the_norm_kernel_needs_no_issued_count(W, NS):
+    rng = random.Random(W * 10 + NS)
+    for _ in range(300):
+        assert run_broadcast_ring(4 * NS + 3, W, NS, rng) == 0
