@@ -8,8 +8,9 @@ O += P_J V_J and then S_{J+3} = Q K_{J+3}^T into score buffer (J+1) mod 2);
 the softmax reads S_J, publishes P_J into a single P buffer once
 O += P_{J-1} V_{J-1} has completed, writes the next unit's Q once the current
 unit's last score tile is read, and reads O at each unit's end.  mbarrier
-waits are parity waits (pass iff completed phases % 2 != parity); each MMA
-thread's tensor-core operations complete in its own issue order; bulk copies
+waits are parity waits (pass iff completed phases % 2 != parity); a
+thread's MMAs complete in issue order only where they share an accumulator,
+and its commits once all it issued before them completed; bulk copies
 complete in any order.  Checked in every interleaving: every product reads
 the stage, score buffer, P and Q it was meant to, the first P V of a unit
 overwrites O only after the previous epilogue read it, nothing deadlocks.
@@ -26,6 +27,24 @@ Without the flag the phase wait could pass on an older fill of the stage."""
 import random
 
 import pytest
+
+
+def take_tensor_op(queue, rng):
+    """Removes and returns one tensor-core operation of a thread that may
+    complete next: MMAs on the same accumulator complete in issue order, others
+    in any order, and a commit (an mbarrier arrive once everything the thread
+    issued before it has completed) only when nothing earlier is pending."""
+    ready = []
+    seen = set()
+    for k, op in enumerate(queue):
+        if op[0] == "commit":
+            if k == 0:
+                ready.append(k)
+            continue
+        if op[-1] not in seen:
+            ready.append(k)
+        seen.add(op[-1])
+    return queue.pop(rng.choice(ready))
 
 
 class Bar:
@@ -123,7 +142,7 @@ def run_pipe(units, seed, nstage, q_handoff="count", pad_tile=None, pad_flag=Tru
             yield lambda: kv_full[sidx].ok(ph)
             if J >= 2:
                 yield lambda: s_read[J & 1].ok(buf_parity(J - 2))
-            queues[p].extend([("qk", J, sidx), ("commit", s_full[J & 1]), ("commit", kv_empty[sidx])])
+            queues[p].extend([("qk", J, sidx, ("S", J & 1)), ("commit", s_full[J & 1]), ("commit", kv_empty[sidx])])
 
         yield from issue_qk(p)
         if p == 1 and N > 2:
@@ -135,7 +154,7 @@ def run_pipe(units, seed, nstage, q_handoff="count", pad_tile=None, pad_flag=Tru
             yield lambda: p_ready[p].ok(buf_parity(J))
             if J == pad_tile:
                 yield lambda: v_clean.ok(0)
-            queues[p].extend([("pv", J, sidx), ("commit", pv_done[p]), ("commit", kv_empty[sidx])])
+            queues[p].extend([("pv", J, sidx, ("O",)), ("commit", pv_done[p]), ("commit", kv_empty[sidx])])
             if J + 3 < N:
                 yield from issue_qk(J + 3)
 
@@ -173,7 +192,7 @@ def run_pipe(units, seed, nstage, q_handoff="count", pad_tile=None, pad_flag=Tru
             useq += 1
 
     def execute(p):
-        op = queues[p].pop(0)
+        op = take_tensor_op(queues[p], rng)
         if op[0] == "commit":
             op[1].arrive()
         elif op[0] == "qk":
@@ -273,4 +292,158 @@ def test_padding_warp_without_the_issue_flag_can_take_an_older_fill():
     # on a fill two rounds older, or be empty, when the padding tile's V is a
     # later fill of its stage
     bad = sum(bool(run_pipe([40], trial, 7, pad_tile=20, pad_flag=False)) for trial in range(200))
+    assert bad > 0
+
+
+def run_two_tile(n_tiles, NQ, nstage, seed, pad_tile=None, wait_pv_before_s=True):
+    """One random interleaving of the two-tile kernel (attn_fwd): NQ query
+    tiles share each K/V tile; the producer loads Q once, then K_j, V_j into
+    an nstage ring; one MMA-issuing thread, per key tile j, waits for K_j and,
+    per query tile q, for O_q += P_q V_{j-1} to complete (P_q lives over S_q)
+    before S_q = Q_q K_j^T, then waits for V_j and each P_q before
+    O_q += P_q V_j; softmax q waits for S_q, may rescale O_q (after waiting for
+    the previous P V of its tile, which skips phases of that barrier), writes
+    P_q over S_q and publishes it; the epilogue waits for the last P V.
+    Returns the list of protocol violations."""
+    rng = random.Random(seed)
+    q_full = Bar()
+    kv_full = [Bar() for _ in range(nstage)]
+    kv_empty = [Bar() for _ in range(nstage)]
+    s_full = [Bar() for _ in range(NQ)]
+    p_ready = [Bar() for _ in range(NQ)]
+    pv_done = [Bar() for _ in range(NQ)]
+    v_clean = Bar()
+    st = {"Q": False, "stage": [None] * nstage, "S": [None] * NQ, "P": [None] * NQ, "O": [0] * NQ,
+          "pad_issued": False, "zeroed": None}
+    queue = []
+    copies = []
+    errors = []
+
+    def producer():
+        copies.append(("Q", None))
+        for ld in range(2 * n_tiles):
+            sidx, ph = ld % nstage, (ld // nstage) & 1
+            yield lambda sidx=sidx, ph=ph: kv_empty[sidx].ok(ph ^ 1)
+            what = ("K" if ld % 2 == 0 else "V", ld // 2)
+            copies.append((sidx, what))
+            if what == ("V", pad_tile):
+                st["pad_issued"] = True
+
+    def pad_warp():
+        ld = 2 * pad_tile + 1
+        sidx, ph = ld % nstage, (ld // nstage) & 1
+        yield lambda: st["pad_issued"]
+        yield lambda: kv_full[sidx].ok(ph)
+        if st["stage"][sidx] != ("V", pad_tile):
+            errors.append(f"padding warp zeroes stage {sidx} holding {st['stage'][sidx]}")
+        st["zeroed"] = pad_tile
+        v_clean.arrive()
+
+    def mma():
+        yield lambda: q_full.ok(0)
+        for j in range(n_tiles):
+            sk, phk = (2 * j) % nstage, ((2 * j) // nstage) & 1
+            yield lambda: kv_full[sk].ok(phk)
+            for q in range(NQ):
+                if j > 0 and wait_pv_before_s:
+                    yield lambda q=q: pv_done[q].ok((j - 1) & 1)
+                queue.extend([("qk", q, j, sk, ("S", q)), ("commit", s_full[q])])
+            queue.append(("commit", kv_empty[sk]))
+            sv, phv = (2 * j + 1) % nstage, ((2 * j + 1) // nstage) & 1
+            yield lambda: kv_full[sv].ok(phv)
+            if j == pad_tile:
+                yield lambda: v_clean.ok(0)
+            for q in range(NQ):
+                yield lambda q=q: p_ready[q].ok(j & 1)
+                queue.extend([("pv", q, j, sv, ("O", q)), ("commit", pv_done[q])])
+            queue.append(("commit", kv_empty[sv]))
+
+    def softmax(q):
+        for j in range(n_tiles):
+            yield lambda: s_full[q].ok(j & 1)
+            if st["S"][q] != j:
+                errors.append(f"softmax {q} reads S holding tile {st['S'][q]} for tile {j}")
+            if j > 0 and rng.random() < 0.5:   # the running max grew: rescale O_q
+                yield lambda: pv_done[q].ok((j - 1) & 1)
+                if st["O"][q] != j:
+                    errors.append(f"softmax {q} rescales O holding {st['O'][q]} tiles at tile {j}")
+            st["P"][q] = j
+            st["S"][q] = None   # P is written over S
+            p_ready[q].arrive()
+        if n_tiles:
+            yield lambda: pv_done[q].ok((n_tiles - 1) & 1)
+            if st["O"][q] != n_tiles:
+                errors.append(f"epilogue {q} reads O holding {st['O'][q]} of {n_tiles} tiles")
+
+    def execute():
+        op = take_tensor_op(queue, rng)
+        if op[0] == "commit":
+            op[1].arrive()
+            return
+        kind, q, j, sidx, _ = op
+        if kind == "qk":
+            if not st["Q"]:
+                errors.append(f"S_{q} of tile {j} reads Q before it landed")
+            if st["stage"][sidx] != ("K", j):
+                errors.append(f"S_{q} of tile {j} reads stage {sidx} holding {st['stage'][sidx]}")
+            if st["P"][q] is not None and st["O"][q] != st["P"][q] + 1:
+                errors.append(f"S_{q} of tile {j} overwrites P of tile {st['P'][q]} before O += P V read it")
+            st["S"][q] = j
+        else:
+            if st["stage"][sidx] != ("V", j):
+                errors.append(f"O_{q} += P V of tile {j} reads stage {sidx} holding {st['stage'][sidx]}")
+            if j == pad_tile and st["zeroed"] != j:
+                errors.append(f"O_{q} += P V of tile {j} reads V before its padding rows were zeroed")
+            if st["P"][q] != j or st["O"][q] != j:
+                errors.append(f"O_{q} += P V of tile {j} reads P {st['P'][q]} onto O of {st['O'][q]} tiles")
+            st["O"][q] = j + 1
+
+    roles = {"producer": producer(), "mma": mma()}
+    roles.update({f"softmax{q}": softmax(q) for q in range(NQ)})
+    if pad_tile is not None:
+        roles["pad"] = pad_warp()
+    waits = {}
+    for name in list(roles):
+        try:
+            waits[name] = next(roles[name])
+        except StopIteration:
+            del roles[name]
+    while roles or queue or copies:
+        moves = [("role", r) for r in roles if waits[r]()]
+        if queue:
+            moves.append(("tensor", None))
+        moves += [("copy", i) for i in range(len(copies))]
+        if not moves:
+            return [f"deadlock: {sorted(roles)} waiting"]
+        kind, x = rng.choice(moves)
+        if kind == "role":
+            try:
+                waits[x] = roles[x].send(None)
+            except StopIteration:
+                del roles[x]
+        elif kind == "tensor":
+            execute()
+        else:
+            sidx, what = copies.pop(x)
+            if sidx == "Q":
+                st["Q"] = True
+                q_full.arrive()
+            else:
+                st["stage"][sidx] = what
+                kv_full[sidx].arrive()
+        if errors:
+            return errors
+    return errors
+
+
+@pytest.mark.parametrize("NQ,nstage", [(1, 2), (1, 4), (2, 4), (2, 8), (1, 2)])
+def test_two_tile_kernel_protocol_is_clean(NQ, nstage):
+    for n in (1, 2, 5, 16):
+        for trial in range(60):
+            pad = None if trial % 3 == 0 else trial % n
+            assert run_two_tile(n, NQ, nstage, trial, pad_tile=pad) == [], f"n {n}, pad {pad}, seed {trial}"
+
+
+def test_two_tile_kernel_needs_the_wait_before_the_next_score_product():
+    bad = sum(bool(run_two_tile(8, 2, 4, trial, wait_pv_before_s=False)) for trial in range(300))
     assert bad > 0
