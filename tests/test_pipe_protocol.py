@@ -23,7 +23,12 @@ skips a one-tile unit can no longer tell unit k's Q from unit k - 2's.
 The padding warp (one unit per CTA) zeroes the V rows past kv_len of the key
 tile that straddles it: it waits for the producer's flag that the tile's V
 load is issued, then for the stage's phase, and the tile's P V waits for it.
-Without the flag the phase wait could pass on an older fill of the stage."""
+Without the flag the phase wait could pass on an older fill of the stage.
+
+run_two_tile models the two-tile kernel (one MMA-issuing thread, NQ query
+tiles sharing each K/V tile, P_q written over S_q): the issuer's wait for
+O_q += P_q V before the next S_q is what keeps S_q from overwriting an unread
+P_q, since the two products write different accumulators."""
 import random
 
 import pytest
