@@ -96,7 +96,11 @@ typedef struct {
  * The float32 operation order is fixed (lane partial sums of 8 channels,
  * butterfly across lanes, correctly rounded sqrt and divide, separate
  * multiplies, fused multiply-adds in the rotation, round-to-nearest-even
- * stores), so results are reproducible bit for bit.
+ * stores), so results are reproducible bit for bit.  Any even rotary_dim is
+ * accepted; multiples of 16 (96 of 128 in H3) take the fast path in which a
+ * lane holds whole rotation pairs, other values a slower path that rotates
+ * channel by channel through shared memory (same results bit for bit as the
+ * fixed order above).
  *
  * q: [B, S, Hq, D] bf16, k: [B, S, Hkv, D] bf16 (device, in place, must not
  *    overlap each other).  Either may be NULL with its head count 0 to
@@ -104,8 +108,9 @@ typedef struct {
  * wq, wk: [D] float32 RMSNorm weights (device), shared by all heads.
  * cos, sin: [S, rotary_dim/2] float32 (device); row = sequence position.
  *    May be NULL when rotary_dim == 0.
- * D in {64, 128, 256}; rotary_dim a multiple of 16 with 0 <= rotary_dim <= D;
- * eps >= 0 and finite.  Pointers 16-byte aligned (tables and weights 4-byte).
+ * D in {64, 128, 256}; rotary_dim even with 0 <= rotary_dim <= D;
+ * eps >= 0 and finite.  Every pointer 16-byte aligned (rows, weights and
+ * tables alike).
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_HEAD_DIM, UNSUPPORTED_DEVICE,
  * LAUNCH.
  */
@@ -144,7 +149,8 @@ h3attn_status_t h3attn_qk_norm_rope_out(const void* q, const void* k, void* q_ou
  * q: [B, Sq, Hq, D] bf16; k, v: [B, Sk, Hkv, D] bf16; o: [B, Sq, Hq, D] bf16
  *    (all device; o must not overlap q, k or v).  Query head h reads key/value
  *    head h / (Hq / Hkv) (GQA, contiguous groups).
- * scale: finite, >= 0 (typically 1/sqrt(D)).
+ * scale: finite and > 0 (typically 1/sqrt(D)); 0, negative or non-finite
+ *    values are rejected (INVALID_ARG).
  * mask: NULL (dense) or a descriptor as above.  causal: nonzero applies the
  *    causal mask to every sample; causal masking requires Sq == Sk.
  * D in {64, 128, 256}; Hq % Hkv == 0; B, Sq, Sk, Hq, Hkv >= 1 (B*Sq == 0 is
@@ -228,10 +234,17 @@ h3attn_status_t h3attn_prefill_window(const void* q, const void* k, const void* 
 const char* h3attn_status_string(h3attn_status_t status);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's status
- * word.  Returns H3ATTN_ERR_TIMEOUT if any kernel since the last check gave
- * up on a bounded wait, H3ATTN_ERR_LAUNCH if the stream reports a CUDA error,
- * else H3ATTN_OK.
+ * Synchronises `stream`, then reads the current device's status word and
+ * clears it.  Returns H3ATTN_ERR_TIMEOUT if a kernel gave up on a bounded wait
+ * (H3ATTN_ERR_INVALID_ARG for an out-of-range modulation index) since the
+ * last check, H3ATTN_ERR_LAUNCH if the stream reports a CUDA error, else
+ * H3ATTN_OK.
+ * The status word is one per device, shared by every stream and host thread
+ * on it: a kernel on any stream can set it, and a check on any stream reports
+ * it.  The read and the clear are issued on `stream` (after its work), and the
+ * word is cleared only if it still holds the value read, so a report that
+ * another stream's kernel writes in between is kept for the next check rather
+ * than lost.  The word holds one code; several reports before a check merge.
  */
 h3attn_status_t h3attn_check_device_status(h3attn_stream_t stream);
 

@@ -134,7 +134,7 @@ def qk_norm_rope_emulate(x, w, cos, sin, rotary_dim, eps, nthreads=0):
     B, S, H, D = x.shape
     _check_rows(x, D)
     assert D % 16 == 0 and D // 16 <= 32 and (D // 16) & (D // 16 - 1) == 0
-    assert rotary_dim % 16 == 0 and rotary_dim <= D
+    assert rotary_dim % 2 == 0 and 0 <= rotary_dim <= D
     half = rotary_dim // 2
     w = np.ascontiguousarray(w, dtype=np.float32)
     cos = np.ascontiguousarray(cos, dtype=np.float32).reshape(-1, half) if half else np.zeros((S, 1), np.float32)

@@ -196,10 +196,11 @@ void oracle_qk_norm_rope_f64(const uint16_t* x, double* y, int64_t rows, int S, 
 /* ------------------------------------------------------------------ */
 /* The same step in float32 with a fixed operation order (the bit-exact  */
 /* contract for a CUDA implementation):                                  */
-/*   8-channel groups g = 0 .. D/8-1; h8 = rotary_dim/16 groups per      */
-/*   rotated half; L = D/16 lanes, each holding two groups: first group   */
-/*   g0 = l (l < h8) or L + l (l >= h8), second group g1 = l + h8, so a   */
-/*   lane l < h8 holds the rotation pair (l, l + h8);                     */
+/*   8-channel groups g = 0 .. D/8-1; h8 = floor(rotary_dim/16);         */
+/*   L = D/16 lanes, each holding two groups: first group g0 = l (l < h8) */
+/*   or L + l (l >= h8), second group g1 = l + h8 (every group exactly     */
+/*   once for any h8 in 0..L; when 16 divides rotary_dim a lane l < h8    */
+/*   holds the rotation pair (l, l + h8));                                */
 /*   per lane acc = 0; acc = fmaf(x, x, acc) over the 8 channels of g0 in */
 /*   order, then those of g1;                                             */
 /*   butterfly over lanes: for off = L/2 .. 1: p[l] = p[l] + p[l ^ off];   */

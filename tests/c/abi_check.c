@@ -58,7 +58,7 @@ int main(void) {
   EXPECT(h3attn_prefill(q, k, v, o, 1, 256, 256, 4, 4, 128, 0.1f, &mask, 0, NULL), H3ATTN_ERR_MISALIGNED);
 
   /* norm/RoPE: B, S, Hq, Hkv, D, rotary_dim, eps */
-  EXPECT(h3attn_qk_norm_rope(q, k, w, w, cs, cs, 1, 64, 4, 4, 128, 90, 1e-6f, NULL), H3ATTN_ERR_INVALID_ARG);
+  EXPECT(h3attn_qk_norm_rope(q, k, w, w, cs, cs, 1, 64, 4, 4, 128, 91, 1e-6f, NULL), H3ATTN_ERR_INVALID_ARG); /* odd */
   EXPECT(h3attn_qk_norm_rope(q, k, w, w, cs, cs, 1, 64, 4, 4, 100, 96, 1e-6f, NULL), H3ATTN_ERR_UNSUPPORTED_HEAD_DIM);
   EXPECT(h3attn_qk_norm_rope(q, k, w, w, NULL, NULL, 1, 64, 4, 4, 128, 96, 1e-6f, NULL), H3ATTN_ERR_INVALID_ARG);
   EXPECT(h3attn_qk_norm_rope(q, q, w, w, cs, cs, 1, 64, 4, 4, 128, 96, 1e-6f, NULL), H3ATTN_ERR_INVALID_ARG);

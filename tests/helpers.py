@@ -84,3 +84,10 @@ def assert_convex_bound(dv, do, group: int, what: str):
     bound = vmax.repeat_interleave(group, dim=1)[:, None]        # [B, 1, Hq, D]
     over = o.abs() > bound * 1.01 + 1e-6
     assert not bool(over.any()), f"{what}: {int(over.sum())} outputs exceed the value range of their column"
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (8 significant bits; 2^-133 at zero)."""
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)

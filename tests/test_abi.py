@@ -88,7 +88,8 @@ def norm(lib, q=FAKE, k=FAKE * 64, wq=FAKE * 200, wk=FAKE * 201, cos=FAKE * 202,
 
 def test_norm_rope_validation(lib):
     assert norm(lib, D=80) == h3.H3ATTN_ERR_UNSUPPORTED_HEAD_DIM
-    assert norm(lib, rot=100) == h3.H3ATTN_ERR_INVALID_ARG  # not a multiple of 16
+    assert norm(lib, rot=95) == h3.H3ATTN_ERR_INVALID_ARG  # odd
+    assert norm(lib, rot=-2) == h3.H3ATTN_ERR_INVALID_ARG
     assert norm(lib, rot=144) == h3.H3ATTN_ERR_INVALID_ARG  # > D
     assert norm(lib, eps=-1.0) == h3.H3ATTN_ERR_INVALID_ARG
     assert norm(lib, eps=float("inf")) == h3.H3ATTN_ERR_INVALID_ARG

@@ -6,9 +6,10 @@ import pytest
 
 import h3inputs as gen
 import oracle
-from helpers import from_dev, to_dev, to_dev_f32
+from helpers import bf16_f64, bf16_ulp, from_dev, to_dev, to_dev_f32
 
-NORM_WORKLOADS = ["tiny_mha", "dit_block", "long_video_h12", "padded_gqa", "packed_clip_self"]
+NORM_WORKLOADS = ["tiny_mha", "dit_block", "long_video_h12", "long_video_h24", "padded_gqa",
+                  "packed_clip_self"]
 
 
 def _run(h3, q_bits, k_bits, wq, wk, cos, sin, rot, eps):
@@ -76,6 +77,39 @@ def test_bit_exact_edge_shapes(h3, D, rot, eps, B, S, Hq, Hkv):
     gq, gk = _run(h3, q, k, wq, wk, cos, sin, rot, eps)
     _assert_bits_equal(gq, oracle.qk_norm_rope_emulate(q, wq, cos, sin, rot, eps), "q")
     _assert_bits_equal(gk, oracle.qk_norm_rope_emulate(k, wk, cos, sin, rot, eps), "k")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,rot", [(128, 2), (128, 24), (128, 40), (128, 94), (64, 2), (64, 62),
+                                   (256, 18), (256, 250)])
+def test_any_even_rotary_dim(h3, D, rot):
+    """rotary_dim even but not a multiple of 16: rotation pairs straddle the
+    lanes' channel groups (the kernel's channel-by-channel path).  Bit-exact
+    against the emulation, within the emulation's rounding bound of the fp64
+    definition, and the out-of-place call bit-equal to the in-place one."""
+    B, S, Hq, Hkv = 2, 41, 3, 1
+    q = gen.normal_bshd(B, S, Hq, D, 13, gen.STREAM_Q, 1.0, 0.5)
+    k = gen.normal_bshd(B, S, Hkv, D, 13, gen.STREAM_K)
+    wq = gen.uniform_f32(D, 13, gen.STREAM_WQ, 0.5, 1.5)
+    wk = gen.uniform_f32(D, 13, gen.STREAM_WK, 0.5, 1.5)
+    cos, sin = gen.rope_tables(S, rot)
+    gq, gk = _run(h3, q, k, wq, wk, cos, sin, rot, 1e-6)
+    eq = oracle.qk_norm_rope_emulate(q, wq, cos, sin, rot, 1e-6)
+    _assert_bits_equal(gq, eq, f"q rot {rot}")
+    _assert_bits_equal(gk, oracle.qk_norm_rope_emulate(k, wk, cos, sin, rot, 1e-6), f"k rot {rot}")
+    # |gpu - fp64| <= ulp(y) + 2 ulp(|(a, b)|): a boundary value one bf16 step
+    # off, carried through the rotation by the pair's magnitude, plus the store
+    exact = oracle.qk_norm_rope_f64(q, wq, cos, sin, rot, 1e-6)
+    n = oracle.qk_norm_rope_f64(q, wq, None, None, 0, 1e-6)
+    half = rot // 2
+    mag = np.abs(n).copy()
+    pair = np.sqrt(n[..., :half] ** 2 + n[..., half:rot] ** 2)
+    mag[..., :half] = pair
+    mag[..., half:rot] = pair
+    assert np.all(np.abs(bf16_f64(gq) - exact) <= bf16_ulp(exact) + 2.0 * bf16_ulp(mag))
+    _, _, oq, ok_ = _run_out(h3, q, k, wq, wk, cos, sin, rot, 1e-6)
+    _assert_bits_equal(oq, gq, f"q_out rot {rot}")
+    _assert_bits_equal(ok_, gk, f"k_out rot {rot}")
 
 
 @pytest.mark.gpu

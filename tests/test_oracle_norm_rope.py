@@ -146,7 +146,9 @@ def test_positions_follow_sequence_index_not_head_or_batch():
                 np.testing.assert_array_equal(one[0, 0, 0], y[b, pos, h])
 
 
-@pytest.mark.parametrize("Dd,Rr", [(128, 96), (64, 32), (256, 96), (128, 128), (128, 0)])
+@pytest.mark.parametrize("Dd,Rr", [(128, 96), (64, 32), (256, 96), (128, 128), (128, 0),
+                                   # rotary_dim even but not a multiple of 16
+                                   (128, 2), (128, 24), (128, 40), (128, 94), (64, 62), (256, 250)])
 def test_emulation_within_rounding_bound_of_fp64(Dd, Rr):
     B, S, H = 2, 96, 4
     half = Rr // 2

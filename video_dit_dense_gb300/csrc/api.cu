@@ -6,7 +6,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
-#include <mutex>
+#include <atomic>
 
 #include "internal.h"
 
@@ -14,38 +14,41 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-struct DeviceInfo {
-  std::once_flag once;
-  bool supported = false;
-};
-DeviceInfo g_dev[kMaxDevices];
+// Per device: 0 = not yet known, 1 = supported, 2 = not supported.  Stored
+// only after both attribute queries succeeded, so a failed query is retried
+// on the next call instead of marking the device unsupported for good.
+std::atomic<int> g_dev_state[kMaxDevices];
 
 // Gate on compute capability 10.3 (the only target the kernels are built for).
 h3attn_status_t check_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return H3ATTN_ERR_LAUNCH;
   if (dev < 0 || dev >= kMaxDevices) return H3ATTN_ERR_UNSUPPORTED_DEVICE;
-  std::call_once(g_dev[dev].once, [dev]() {
+  int state = g_dev_state[dev].load(std::memory_order_acquire);
+  if (state == 0) {
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return;
-    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return;
-    g_dev[dev].supported = (major == 10 && minor == 3);
-  });
-  return g_dev[dev].supported ? H3ATTN_OK : H3ATTN_ERR_UNSUPPORTED_DEVICE;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return H3ATTN_ERR_LAUNCH;
+    state = (major == 10 && minor == 3) ? 1 : 2;
+    g_dev_state[dev].store(state, std::memory_order_release);  // racing callers store the same value
+  }
+  return state == 1 ? H3ATTN_OK : H3ATTN_ERR_UNSUPPORTED_DEVICE;
 }
 
+// The driver's tensor-map encoder, looked up until a lookup succeeds.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, []() {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+  if (f) return f;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  fn.store(f, std::memory_order_release);
+  return f;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -113,7 +116,7 @@ h3attn_status_t norm_rope(const void* q, const void* k, void* q_out, void* k_out
                           int D, int rotary_dim, float eps, h3attn_stream_t stream) {
   if (B < 0 || S < 0 || Hq < 0 || Hkv < 0) return H3ATTN_ERR_INVALID_ARG;
   if (!head_dim_ok(D)) return H3ATTN_ERR_UNSUPPORTED_HEAD_DIM;
-  if (rotary_dim < 0 || rotary_dim > D || rotary_dim % 16 != 0) return H3ATTN_ERR_INVALID_ARG;
+  if (rotary_dim < 0 || rotary_dim > D || rotary_dim % 2 != 0) return H3ATTN_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || !isfinite(eps)) return H3ATTN_ERR_INVALID_ARG;
   if ((q == nullptr) != (Hq == 0) || (k == nullptr) != (Hkv == 0)) return H3ATTN_ERR_INVALID_ARG;
   if ((q_out == nullptr) != (q == nullptr) || (k_out == nullptr) != (k == nullptr)) return H3ATTN_ERR_INVALID_ARG;
@@ -313,9 +316,10 @@ h3attn_status_t h3attn_rmsnorm_modulate(const void* x, void* y, const float* w, 
 }
 
 h3attn_status_t h3attn_check_device_status(h3attn_stream_t stream) {
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return H3ATTN_ERR_LAUNCH;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return H3ATTN_ERR_LAUNCH;
   int v = 0;
-  if (h3::read_and_clear_status(&v) != 0) return H3ATTN_ERR_LAUNCH;
+  if (h3::read_and_clear_status(s, &v) != 0) return H3ATTN_ERR_LAUNCH;
   return v == 0 ? H3ATTN_OK : static_cast<h3attn_status_t>(v);
 }
 

@@ -593,13 +593,21 @@ int* status_word_ptr() {
   return cache[dev];
 }
 
-// Reads and clears the current device's status word (synchronous copies).
-int read_and_clear_status(int* value) {
+namespace {
+// Clears the status word if it still holds `seen`: a report that another
+// stream's kernel wrote after the read is kept for the next check.
+__global__ void clear_status_if_kernel(int seen) { atomicCAS(&g_status_word, seen, 0); }
+}  // namespace
+
+// The read and the conditional clear both run in the order of `stream`.
+int read_and_clear_status(cudaStream_t stream, int* value) {
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return 1;
+  if (cudaMemcpyFromSymbolAsync(&v, g_status_word, sizeof(int), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return 1;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return 1;
   if (v != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return 1;
+    clear_status_if_kernel<<<1, 1, 0, stream>>>(v);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess) return 1;
   }
   *value = v;
   return 0;

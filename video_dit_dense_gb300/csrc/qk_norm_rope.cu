@@ -31,6 +31,15 @@
 //   y_{i+h} = fma(b, c, a*s); store bf16(y) (round to nearest even).
 // Explicit round-to-nearest intrinsics and packed f32x2 instructions (each
 // lane rounded once) keep the compiler from contracting or reassociating.
+//
+// rotary_dim need only be even.  When it is not a multiple of 16 (h8 =
+// floor(rotary_dim/16) in the partition above), a rotation pair can straddle
+// two lanes' groups, so that instantiation (GEN) writes each row's boundary
+// values n^ to a per-warp shared-memory row, then every lane rotates its 16
+// channels one at a time with the partner read from that row and the
+// coefficients read from global memory (same formulas, same rounding).  The
+// GEN instantiation never stages table rows; its row buffers use the space
+// of the table slots.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -83,9 +92,11 @@ __device__ __forceinline__ void chunk_of(const NormRopeArgs& a, uint32_t c, uint
   nrows = min(rows_per_chunk, limit - row0);
 }
 
-template <int D>
+template <int D, bool GEN>
 __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __grid_constant__ NormRopeArgs a) {
   using C = NormCfg<D>;
+  // GEN: a warp's row buffer (RPW rows of D bf16) fits in its share of the table slots
+  static_assert(kComputeWarps * (32 / (D / 16)) * D * 2 <= kTabSlots * C::kSlotBytes, "GEN row buffers");
   constexpr int LPR = C::LPR, RPW = C::RPW, U = kUnroll;
   constexpr float kInvD = 1.0f / static_cast<float>(D);
   static_assert(LPR >= U, "each row needs a lane per unrolled row for the shared sqrt/div pass");
@@ -138,7 +149,7 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
         const uint16_t* src = (is_q ? a.q_in : a.k_in) + static_cast<size_t>(row0) * D;
         uint32_t tok0, ntok;
         chunk_tokens(is_q, row0, nrows, tok0, ntok);
-        const bool staged = half > 0 && ntok <= static_cast<uint32_t>(C::kTabTokens) && ntok <= a.div_s.d;
+        const bool staged = !GEN && half > 0 && ntok <= static_cast<uint32_t>(C::kTabTokens) && ntok <= a.div_s.d;
         const uint32_t tab_bytes = staged ? ntok * half * 4 : 0u;
         const uint32_t stage = sbase + st * kChunkBytes;
         const uint32_t slot_c = sbase + C::kTabBase + ts * C::kSlotBytes;  // cos rows; sin rows follow
@@ -196,7 +207,7 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
     const float* tab_s = tab_c + C::kTabBytes / 4;
     uint32_t tok0, ntok;
     chunk_tokens(is_q, row0, nrows, tok0, ntok);
-    const bool staged = half > 0 && ntok <= static_cast<uint32_t>(C::kTabTokens) && ntok <= a.div_s.d;
+    const bool staged = !GEN && half > 0 && ntok <= static_cast<uint32_t>(C::kTabTokens) && ntok <= a.div_s.d;
 
     uint4 xa[U], xb[U];
     uint32_t lrow[U];
@@ -252,7 +263,8 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
     uint16_t* gbase = is_q ? a.q_out : a.k_out;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (lrow[u] >= nrows) continue;
+      const bool live = lrow[u] < nrows;
+      if (!GEN && !live) continue;  // GEN: every lane takes part in the row buffer's warp syncs
       const uint32_t xw[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w, xb[u].x, xb[u].y, xb[u].z, xb[u].w};
       // boundary values n^ = bf16((x * r) * w), kept as bf16 pairs
       uint32_t nb[8];
@@ -265,7 +277,30 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
       }
       const uint32_t r = row0 + lrow[u];
       uint32_t ob[8] = {nb[0], nb[1], nb[2], nb[3], nb[4], nb[5], nb[6], nb[7]};
-      if (rotating) {
+      if constexpr (GEN) {
+        // Row buffer of this warp's row slot: the whole row of n^ values.
+        uint16_t* wrow = reinterpret_cast<uint16_t*>(smem + C::kTabBase) + (warp * RPW + slot) * D;
+        *reinterpret_cast<uint4*>(wrow + g0 * 8) = make_uint4(nb[0], nb[1], nb[2], nb[3]);
+        *reinterpret_cast<uint4*>(wrow + g1 * 8) = make_uint4(nb[4], nb[5], nb[6], nb[7]);
+        __syncwarp();
+        const uint32_t tok = fdiv(r, dh);
+        const size_t pos = tok - fdiv(tok, a.div_s) * a.div_s.d;
+        const int rot = 2 * half;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int d = static_cast<int>((e < 8 ? g0 : g1) * 8) + (e & 7);
+          if (!live || d >= rot) continue;
+          const int i = d < half ? d : d - half;  // pair (n_i, n_{i+half})
+          const float av = __uint_as_float(static_cast<uint32_t>(wrow[i]) << 16);
+          const float bv = __uint_as_float(static_cast<uint32_t>(wrow[i + half]) << 16);
+          const float cs = __ldg(a.cos + pos * half + i), sn = __ldg(a.sin + pos * half + i);
+          const float y = d < half ? __fmaf_rn(av, cs, -__fmul_rn(bv, sn)) : __fmaf_rn(bv, cs, __fmul_rn(av, sn));
+          const uint32_t yb = pack_bf16(y, 0.0f) & 0xFFFFu;
+          uint32_t& word = ob[(e >> 1)];
+          word = (e & 1) ? ((word & 0xFFFFu) | (yb << 16)) : ((word & 0xFFFF0000u) | yb);
+        }
+        __syncwarp();  // the row buffer is rewritten by the next unrolled row
+      } else if (rotating) {
         const uint32_t tok = fdiv(r, dh);
         float4 c0, c1, s0, s1;
         if (staged) {
@@ -301,6 +336,7 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
           ob[4 + e] = pack_bf16(z0, z1);
         }
       }
+      if (!live) continue;
       uint16_t* orow = gbase + static_cast<size_t>(r) * D;
       *reinterpret_cast<uint4*>(orow + g0 * 8) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
       *reinterpret_cast<uint4*>(orow + g1 * 8) = make_uint4(ob[4], ob[5], ob[6], ob[7]);
@@ -310,7 +346,7 @@ __global__ void __launch_bounds__(kNormThreads, 3) qk_norm_rope_kernel(const __g
   }
 }
 
-template <int D>
+template <int D, bool GEN>
 cudaError_t launch_d(const NormRopeArgs& a, cudaStream_t stream) {
   using C = NormCfg<D>;
   static bool attr_set[64] = {};
@@ -318,7 +354,7 @@ cudaError_t launch_d(const NormRopeArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(qk_norm_rope_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    e = cudaFuncSetAttribute(qk_norm_rope_kernel<D, GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -330,17 +366,18 @@ cudaError_t launch_d(const NormRopeArgs& a, cudaStream_t stream) {
   int64_t blocks = static_cast<int64_t>(sms) * 3;  // three resident CTAs per SM
   if (blocks > chunks) blocks = chunks;
   if (blocks == 0) return cudaSuccess;
-  qk_norm_rope_kernel<D><<<static_cast<unsigned>(blocks), kNormThreads, C::kSmem, stream>>>(a);
+  qk_norm_rope_kernel<D, GEN><<<static_cast<unsigned>(blocks), kNormThreads, C::kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_qk_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
+  const bool gen = (a.rotary_dim % 16) != 0;  // rotation pairs may straddle two lanes
   switch (a.D) {
-    case 64: return launch_d<64>(a, stream);
-    case 128: return launch_d<128>(a, stream);
-    case 256: return launch_d<256>(a, stream);
+    case 64: return gen ? launch_d<64, true>(a, stream) : launch_d<64, false>(a, stream);
+    case 128: return gen ? launch_d<128, true>(a, stream) : launch_d<128, false>(a, stream);
+    case 256: return gen ? launch_d<256, true>(a, stream) : launch_d<256, false>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
