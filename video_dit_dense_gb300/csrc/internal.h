@@ -10,8 +10,10 @@
 
 namespace h3 {
 
-// Reads and clears the current device's status word (see h3attn_check_device_status).
-int read_and_clear_status(int* value);
+// Reads the current device's status word in the order of `stream`, then
+// clears it only if it still holds the value read (see
+// h3attn_check_device_status).  Returns nonzero on a CUDA error.
+int read_and_clear_status(cudaStream_t stream, int* value);
 // Device address of the current device's status word (nullptr on failure).
 int* status_word_ptr();
 
