@@ -213,11 +213,13 @@ def run_gpu(args):
         mask = h3.Mask(kv_len=None if inp.kv_len is None else torch.from_numpy(inp.kv_len).cuda(),
                        causal_b=None if inp.causal_b is None else torch.from_numpy(inp.causal_b).cuda())
     stream = torch.cuda.current_stream()
+    # the split-key tail's workspace (caller-owned; None when the shape does not split)
+    wsp = h3.prefill_workspace(q, k, mask) if args.split else None
 
     def step():
         if wl.norm_rope:
             h3.h3attn_qk_norm_rope(q, kn, wq, wkn, cos, sin, wl.rotary_dim, wl.eps, stream)
-        h3.h3attn_prefill(q, k, v, o, wl.scale, mask, False, stream)
+        h3.h3attn_prefill(q, k, v, o, wl.scale, mask, False, stream, workspace=wsp)
 
     def barrier():
         if ws > 1:
@@ -241,7 +243,7 @@ def run_gpu(args):
         if wl.norm_rope:
             h3.h3attn_qk_norm_rope(q, kn, wq, wkn, cos, sin, wl.rotary_dim, wl.eps, stream)
         ev[i][1].record(stream)
-        h3.h3attn_prefill(q, k, v, o, wl.scale, mask, False, stream)
+        h3.h3attn_prefill(q, k, v, o, wl.scale, mask, False, stream, workspace=wsp)
         ev[i][2].record(stream)
     t_end.record(stream)
     barrier()
@@ -278,7 +280,7 @@ def run_gpu(args):
             stream.wait_event(ev_out[i % 2])
         if wl.norm_rope:
             h3.h3attn_qk_norm_rope(bq, None if wl.cross else bk, wq, wkn, cos, sin, wl.rotary_dim, wl.eps, stream)
-        h3.h3attn_prefill(bq, bk, bv, bo, wl.scale, mask, False, stream)
+        h3.h3attn_prefill(bq, bk, bv, bo, wl.scale, mask, False, stream, workspace=wsp)
         ev_done[i % 2].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_done[i % 2])
@@ -315,6 +317,13 @@ def run_gpu(args):
     # recorded traffic is for the default workload's launches only
     traffic = _profiled_traffic() if wl.name == WORKLOAD else {}
     attn_kernel = _attn_kernel_name(wl)
+    if wsp is not None:
+        attn_kernel += " (split-key tail) + split_combine_kernel<%d>" % wl.D
+    attn_launches = 2 if wsp is not None else 1
+    # the dense bf16 tensor rate at the clock the kernel ran at: 152 SMs x 8192
+    # flop (4096 bf16 FMA) per clock per SM x the median SM clock of the timed region
+    sm_mhz = (clk or {}).get("sm_mhz")
+    clock_peak = 152 * 8192 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
     masks = []
     if inp.kv_len is not None:
         masks.append("key padding kv_len=%s" % list(map(int, inp.kv_len)))
@@ -352,7 +361,7 @@ def run_gpu(args):
             "d2h_bytes_per_step": int(ho.numel() * 2),
             "ms_per_step": round(e2e_ms / args.steps, 4),
         },
-        "gpu_launches": (2 if wl.norm_rope else 1) * args.steps,
+        "gpu_launches": ((1 if wl.norm_rope else 0) + attn_launches) * args.steps,
         "roofline": {
             "kernel": attn_kernel,
             "bound": "tensor",
@@ -361,6 +370,8 @@ def run_gpu(args):
             "unit": "TFLOP/s",
             "frac": round(attn_tflops / peaks["bf16_tflops"], 4),
             "frac_of_sustained": round(attn_tflops / peaks["bf16_tflops_sustained"], 4),
+            "frac_of_clock_peak": None if clock_peak is None else round(attn_tflops / clock_peak, 4),
+            "clock_peak_how": "152 SMs x 8192 bf16 flop/clk x median SM MHz in the timed region",
             "peak_source": peaks["source"] + " burst bf16 (MEASURED_PEAKS.json)",
             "traffic": traffic.get("attn"),
             "ms_per_launch": round(attn_ms, 4),
@@ -627,6 +638,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-modulate", dest="modulate", action="store_false", default=True,
                     help="skip the RMSNorm -> AdaLN modulation measurement")
+    ap.add_argument("--no-split", dest="split", action="store_false", default=True,
+                    help="run prefill without the split-key tail's workspace")
     ap.add_argument("--no-window", dest="window", action="store_false", default=True,
                     help="skip the chunked-window attention measurement")
     args = ap.parse_args()

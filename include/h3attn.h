@@ -26,6 +26,7 @@
 #ifndef H3ATTN_H_
 #define H3ATTN_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -168,6 +169,48 @@ h3attn_status_t h3attn_qk_norm_rope_out(const void* q, const void* k, void* q_ou
 h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Sq,
                                int Sk, int Hq, int Hkv, int D, float scale,
                                const h3attn_mask_t* mask, int causal, h3attn_stream_t stream);
+
+/*
+ * Dense prefill attention as h3attn_prefill(), with a caller-owned workspace
+ * for the split-key tail.  The work units (128 query rows of one batch item
+ * and head) of a long-sequence call are equal in length, and the last
+ * (units mod number-of-SMs) of them would run as a partial wave of their own
+ * while the other SMs idle.  With a workspace those last units are cut into
+ * key ranges that run side by side on the idle SMs; each range writes its
+ * unnormalised output, running max and row sum to the workspace, and a
+ * combine kernel merges the ranges of a unit in a fixed order
+ * (o = sum 2^(m_i - M) O_i / sum 2^(m_i - M) l_i, M = max m_i), so results
+ * are deterministic.  This is the split-key (O, m, l) combination of the
+ * online softmax over key blocks; the pages' own kernels run one launch per
+ * batch item (FastVideo PR #1799 "Add opt-in FlashInfer attention backend for
+ * Wan", section "Implementation": single prefill per item) and pack batch-1
+ * long sequences (FastVideo PR #1832, section "Performance considerations").
+ *
+ * workspace: device memory of at least h3attn_prefill_workspace_size() bytes
+ *    for the same arguments, 16-byte aligned, not overlapping q, k, v or o;
+ *    its contents on entry do not matter and are overwritten.  NULL (or a
+ *    size of 0 from the query) runs the call exactly as h3attn_prefill().
+ *    Calls that share a workspace must be ordered (one stream, or events):
+ *    the tail of one call and the combine of another would race on it.
+ * The split applies to the head-dim-128 kernel from 1024 keys (and to head
+ * dim 64 when that kernel is forced), without causal masks.  Other arguments
+ * and errors as for h3attn_prefill(); a workspace smaller than required is
+ * INVALID_ARG.
+ */
+h3attn_status_t h3attn_prefill_ws(const void* q, const void* k, const void* v, void* o, int B, int Sq,
+                                  int Sk, int Hq, int Hkv, int D, float scale,
+                                  const h3attn_mask_t* mask, int causal, void* workspace,
+                                  size_t workspace_bytes, h3attn_stream_t stream);
+
+/*
+ * Workspace bytes h3attn_prefill_ws() needs for these arguments on the
+ * current device (0 when the call would not split), written to *bytes.  The
+ * size depends on the device's SM count; it is at most
+ * SMs * 128 * (D + 2) * 4 bytes (10.1 MB for head dim 128 on 152 SMs).
+ * Errors: INVALID_ARG, UNSUPPORTED_HEAD_DIM, UNSUPPORTED_DEVICE, LAUNCH.
+ */
+h3attn_status_t h3attn_prefill_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                                              const h3attn_mask_t* mask, int causal, size_t* bytes);
 
 /*
  * Fused RMSNorm -> indexed AdaLN scale/shift modulation of DiT hidden rows

@@ -190,3 +190,23 @@ class _GradEnabledBf16:
 
     def dim(self):
         return 4
+
+
+def test_workspace_entry_points_validation(lib):
+    n = ctypes.c_size_t(123)
+    ws = lib.h3attn_prefill_workspace_size
+    assert ws(1, 256, 256, 4, 4, 96, None, 0, ctypes.byref(n)) == h3.H3ATTN_ERR_UNSUPPORTED_HEAD_DIM
+    assert n.value == 0  # cleared before any check that fails
+    assert ws(1, 256, 0, 4, 4, 128, None, 0, ctypes.byref(n)) == h3.H3ATTN_ERR_INVALID_ARG
+    assert ws(1, 256, 256, 6, 4, 128, None, 0, ctypes.byref(n)) == h3.H3ATTN_ERR_INVALID_ARG
+    assert ws(1, 256, 256, 4, 4, 128, None, 0, None) == h3.H3ATTN_ERR_INVALID_ARG
+    assert ws(0, 256, 256, 4, 4, 128, None, 0, ctypes.byref(n)) == h3.H3ATTN_OK and n.value == 0
+
+    M = 0x100000  # 1 MiB apart: the [1, 256, 4, 128] tensors do not overlap
+
+    def pws(workspace, q=M, o=4 * M, D=128):
+        return lib.h3attn_prefill_ws(q, 2 * M, 3 * M, o, 1, 256, 256, 4, 4, D, 0.088, None, 0,
+                                     workspace, 1 << 20, None)
+    assert pws(5 * M + 8) == h3.H3ATTN_ERR_MISALIGNED
+    assert pws(5 * M, D=96) == h3.H3ATTN_ERR_UNSUPPORTED_HEAD_DIM
+    assert pws(5 * M, q=M + 8) == h3.H3ATTN_ERR_MISALIGNED

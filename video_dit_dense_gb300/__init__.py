@@ -47,8 +47,9 @@ H3ATTN_ERR_LAUNCH = 6
 H3ATTN_ERR_TIMEOUT = 7
 
 # Every symbol include/h3attn.h declares.
-EXPORTED = ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_prefill_window",
-            "h3attn_rmsnorm_modulate", "h3attn_status_string", "h3attn_check_device_status", "h3attn_version")
+EXPORTED = ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_prefill_ws",
+            "h3attn_prefill_workspace_size", "h3attn_prefill_window", "h3attn_rmsnorm_modulate",
+            "h3attn_status_string", "h3attn_check_device_status", "h3attn_version")
 
 
 class H3AttnError(RuntimeError):
@@ -96,6 +97,12 @@ def load(path: str = LIB_PATH):
             lib.h3attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, F,
                                            ctypes.POINTER(h3attn_mask_t), I, P]
             lib.h3attn_prefill.restype = I
+            lib.h3attn_prefill_ws.argtypes = [P, P, P, P, I, I, I, I, I, I, F,
+                                              ctypes.POINTER(h3attn_mask_t), I, P, ctypes.c_size_t, P]
+            lib.h3attn_prefill_ws.restype = I
+            lib.h3attn_prefill_workspace_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(h3attn_mask_t), I,
+                                                          ctypes.POINTER(ctypes.c_size_t)]
+            lib.h3attn_prefill_workspace_size.restype = I
             lib.h3attn_prefill_window.argtypes = [P, P, P, P, I, I, I, I, I, F, ctypes.POINTER(h3attn_window_t),
                                                   ctypes.POINTER(h3attn_mask_t), P]
             lib.h3attn_prefill_window.restype = I
@@ -221,8 +228,12 @@ def _mask_struct(mask: Mask, B: int):
     return ctypes.pointer(h3attn_mask_t(_ptr(mask.kv_len), _ptr(mask.q_len), _ptr(mask.causal_b), _ptr(mask.bits)))
 
 
-def h3attn_prefill(q, k, v, o, scale=None, mask: Mask | None = None, causal=False, stream=None):
-    """o <- softmax(q k^T * scale) v on BSHD bf16 tensors (o preallocated)."""
+def h3attn_prefill(q, k, v, o, scale=None, mask: Mask | None = None, causal=False, stream=None, workspace=None):
+    """o <- softmax(q k^T * scale) v on BSHD bf16 tensors (o preallocated).
+
+    workspace: None, or a CUDA tensor of at least h3attn_prefill_workspace_size()
+    bytes for the split-key tail (the call then goes through h3attn_prefill_ws).
+    """
     load()
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
         _check_bf16(name, t)
@@ -243,10 +254,42 @@ def h3attn_prefill(q, k, v, o, scale=None, mask: Mask | None = None, causal=Fals
                 raise H3AttnError(H3ATTN_ERR_INVALID_ARG,
                                   f"bits must be contiguous 32-bit CUDA words of shape [{B}, {Sq}, {W}]")
         mptr = _mask_struct(mask, B)
-    st = _lib.h3attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Sq, Sk, Hq, Hkv, D, float(scale), mptr,
-                             int(bool(causal)), _stream_handle(stream))
-    _raise_if(st, "h3attn_prefill")
+    if workspace is None:
+        st = _lib.h3attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Sq, Sk, Hq, Hkv, D, float(scale), mptr,
+                                 int(bool(causal)), _stream_handle(stream))
+        _raise_if(st, "h3attn_prefill")
+    else:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "workspace must be a contiguous CUDA tensor")
+        nbytes = workspace.numel() * workspace.element_size()
+        st = _lib.h3attn_prefill_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Sq, Sk, Hq, Hkv, D, float(scale), mptr,
+                                    int(bool(causal)), _ptr(workspace), nbytes, _stream_handle(stream))
+        _raise_if(st, "h3attn_prefill_ws")
     return o
+
+
+def h3attn_prefill_workspace_size(B, Sq, Sk, Hq, Hkv, D, mask: Mask | None = None, causal=False) -> int:
+    """Bytes of workspace the split-key tail needs for this call (0: no split).
+    Only the presence of the mask fields matters, not their values."""
+    load()
+    mptr = None
+    if mask is not None:
+        mptr = ctypes.pointer(h3attn_mask_t(_ptr(mask.kv_len), _ptr(mask.q_len), _ptr(mask.causal_b),
+                                            _ptr(mask.bits)))
+    out = ctypes.c_size_t(0)
+    st = _lib.h3attn_prefill_workspace_size(B, Sq, Sk, Hq, Hkv, D, mptr, int(bool(causal)), ctypes.byref(out))
+    _raise_if(st, "h3attn_prefill_workspace_size")
+    return int(out.value)
+
+
+def prefill_workspace(q, k, mask: Mask | None = None, causal=False):
+    """A workspace tensor sized for prefill(q, k, ...) on the current device,
+    or None when the call would not split (allocated by torch: the library
+    allocates nothing)."""
+    import torch
+    B, Sq, Hq, D = q.shape
+    n = h3attn_prefill_workspace_size(B, Sq, k.shape[1], Hq, k.shape[2], D, mask, causal)
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
 
 
 def h3attn_rmsnorm_modulate(x, y, w, scale, shift, idx=None, eps=1e-6, stream=None):

@@ -184,11 +184,37 @@ h3attn_status_t h3attn_qk_norm_rope_out(const void* q, const void* k, void* q_ou
 
 namespace {
 
+// Kernel choice override (tests run every case on every kernel): "1" .. "4".
+int kernel_override() {
+  const char* kern = getenv("H3ATTN_ATTN_KERNEL");
+  return (kern && kern[0] >= '1' && kern[0] <= '4') ? kern[0] - '0' : 0;
+}
+
+// The fields of AttnArgs that decide the kernel and the split-key plan.
+void plan_fields(h3::AttnArgs* a, int B, int Sq, int Sk, int Hq, int Hkv, int D, const h3attn_mask_t* mask,
+                 int causal, const h3attn_window_t* win) {
+  a->B = B;
+  a->Sq = Sq;
+  a->Sk = Sk;
+  a->Hq = Hq;
+  a->Hkv = Hkv;
+  a->D = D;
+  a->causal = causal ? 1 : 0;
+  a->kv_len = mask ? mask->kv_len : nullptr;
+  a->q_len = mask ? mask->q_len : nullptr;
+  a->causal_b = mask ? mask->causal_b : nullptr;
+  a->bits = mask ? mask->bits : nullptr;
+  a->kernel = win ? 1 : kernel_override();  // the window's tile ranges live in the one-query-tile kernel
+  a->win_ct = win ? win->frame_tokens * win->chunk_frames : 0;
+  a->split_full = a->split_tail = a->split_pieces = 0;
+  a->split_ws = nullptr;
+}
+
 // Shared body of the dense and windowed prefill entry points (win == nullptr:
-// dense).
+// dense).  ws: the split-key tail's workspace (nullptr: no split).
 h3attn_status_t prefill(const void* q, const void* k, const void* v, void* o, int B, int Sq, int Sk, int Hq,
                         int Hkv, int D, float scale, const h3attn_mask_t* mask, int causal,
-                        const h3attn_window_t* win, h3attn_stream_t stream) {
+                        const h3attn_window_t* win, void* ws, size_t ws_bytes, h3attn_stream_t stream) {
   if (B < 0 || Sq < 0 || Sk < 1 || Hq < 1 || Hkv < 1) return H3ATTN_ERR_INVALID_ARG;
   if (!head_dim_ok(D)) return H3ATTN_ERR_UNSUPPORTED_HEAD_DIM;
   if (Hq % Hkv != 0) return H3ATTN_ERR_INVALID_ARG;
@@ -220,37 +246,36 @@ h3attn_status_t prefill(const void* q, const void* k, const void* v, void* o, in
   const int64_t nk = static_cast<int64_t>(B) * Sk * Hkv * D * 2;
   if (overlap(o, nq, q, nq) || overlap(o, nq, k, nk) || overlap(o, nq, v, nk))
     return H3ATTN_ERR_INVALID_ARG;
+  if (ws && !aligned16(ws)) return H3ATTN_ERR_MISALIGNED;
   h3attn_status_t st = check_device();
   if (st != H3ATTN_OK) return st;
 
   h3::AttnArgs a;
+  plan_fields(&a, B, Sq, Sk, Hq, Hkv, D, mask, causal, win);
+  if (ws) {
+    const h3::SplitPlan sp = h3::plan_split(a);
+    if (sp.pieces > 0) {
+      const int64_t nb = static_cast<int64_t>(sp.bytes);
+      if (ws_bytes < sp.bytes) return H3ATTN_ERR_INVALID_ARG;
+      if (overlap(ws, nb, q, nq) || overlap(ws, nb, k, nk) || overlap(ws, nb, v, nk) || overlap(ws, nb, o, nq))
+        return H3ATTN_ERR_INVALID_ARG;
+      a.split_full = sp.full;
+      a.split_tail = sp.tail;
+      a.split_pieces = sp.pieces;
+      a.split_ws = static_cast<float*>(ws);
+    }
+  }
   if (!make_bshd_map(&a.tm_q, q, B, Sq, Hq, D) || !make_bshd_map(&a.tm_k, k, B, Sk, Hkv, D) ||
       !make_bshd_map(&a.tm_v, v, B, Sk, Hkv, D))
     return H3ATTN_ERR_LAUNCH;
   a.q_ptr = static_cast<const uint16_t*>(q);
   a.o = static_cast<uint16_t*>(o);
-  a.kv_len = mask ? mask->kv_len : nullptr;
-  a.q_len = mask ? mask->q_len : nullptr;
-  a.causal_b = mask ? mask->causal_b : nullptr;
-  a.bits = mask ? mask->bits : nullptr;
-  a.B = B;
-  a.Sq = Sq;
-  a.Sk = Sk;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.D = D;
-  a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = wait_limit_ns();
   const char* inj = getenv("H3ATTN_FAULT_INJECT_STALL_PRODUCER");
   a.debug_skip_producer = (inj && inj[0] == '1') ? 1 : 0;
-  // Kernel choice override (tests run every case on every kernel): "1" .. "4".
-  const char* kern = getenv("H3ATTN_ATTN_KERNEL");
-  a.kernel = (kern && kern[0] >= '1' && kern[0] <= '4') ? kern[0] - '0' : 0;
-  a.win_ct = a.win_af = a.win_r = 0;
+  a.win_af = a.win_r = 0;
   if (win) {
-    a.kernel = 1;  // the window's tile ranges live in the one-query-tile kernel
-    a.win_ct = win->frame_tokens * win->chunk_frames;
     a.win_af = static_cast<int>(min(static_cast<int64_t>(win->frame_tokens) * win->anchor_frames,
                                     static_cast<int64_t>(Sk)));
     a.win_r = static_cast<int>(min(static_cast<int64_t>(win->radius), static_cast<int64_t>(Sk)));
@@ -266,7 +291,31 @@ extern "C" {
 h3attn_status_t h3attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Sq,
                                int Sk, int Hq, int Hkv, int D, float scale,
                                const h3attn_mask_t* mask, int causal, h3attn_stream_t stream) {
-  return prefill(q, k, v, o, B, Sq, Sk, Hq, Hkv, D, scale, mask, causal, nullptr, stream);
+  return prefill(q, k, v, o, B, Sq, Sk, Hq, Hkv, D, scale, mask, causal, nullptr, nullptr, 0, stream);
+}
+
+h3attn_status_t h3attn_prefill_workspace_size(int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                                              const h3attn_mask_t* mask, int causal, size_t* bytes) {
+  if (!bytes) return H3ATTN_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (B < 0 || Sq < 0 || Sk < 1 || Hq < 1 || Hkv < 1) return H3ATTN_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return H3ATTN_ERR_UNSUPPORTED_HEAD_DIM;
+  if (Hq % Hkv != 0 || B > 65535 || Hq > 65535) return H3ATTN_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(Sq) + 127) / 128 * Hq * B > INT32_MAX) return H3ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return H3ATTN_OK;
+  h3attn_status_t st = check_device();
+  if (st != H3ATTN_OK) return st;
+  h3::AttnArgs a;
+  plan_fields(&a, B, Sq, Sk, Hq, Hkv, D, mask, causal, nullptr);
+  *bytes = h3::plan_split(a).bytes;
+  return H3ATTN_OK;
+}
+
+h3attn_status_t h3attn_prefill_ws(const void* q, const void* k, const void* v, void* o, int B, int Sq, int Sk,
+                                  int Hq, int Hkv, int D, float scale, const h3attn_mask_t* mask, int causal,
+                                  void* workspace, size_t workspace_bytes, h3attn_stream_t stream) {
+  return prefill(q, k, v, o, B, Sq, Sk, Hq, Hkv, D, scale, mask, causal, nullptr, workspace, workspace_bytes,
+                 stream);
 }
 
 h3attn_status_t h3attn_prefill_window(const void* q, const void* k, const void* v, void* o, int B, int S,
@@ -277,7 +326,7 @@ h3attn_status_t h3attn_prefill_window(const void* q, const void* k, const void* 
     const bool ok = win->frame_tokens >= 1 && win->chunk_frames >= 1 && win->anchor_frames >= 0 && win->radius >= 0;
     return ok ? H3ATTN_OK : H3ATTN_ERR_INVALID_ARG;
   }
-  return prefill(q, k, v, o, B, S, S, Hq, Hkv, D, scale, mask, 0, win, stream);
+  return prefill(q, k, v, o, B, S, S, Hq, Hkv, D, scale, mask, 0, win, nullptr, 0, stream);
 }
 
 h3attn_status_t h3attn_rmsnorm_modulate(const void* x, void* y, const float* w, const void* scale,

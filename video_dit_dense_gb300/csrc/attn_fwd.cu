@@ -613,6 +613,35 @@ int read_and_clear_status(cudaStream_t stream, int* value) {
   return 0;
 }
 
+// Split-key tail.  With units of equal length and one resident CTA per SM,
+// the last U mod #SMs units run as a wave of their own while the other SMs
+// idle.  The plan keeps the first U - r units whole and cuts each of the last
+// r units into P = min(#SMs / r, key tiles / 2) key ranges, so that the tail
+// runs on r * P SMs at once.  Only for the one-query-tile kernel's dense
+// path without causal masks (under a causal mask the last units launched are
+// already the shortest ones, and per-sample causal flags are device data).
+SplitPlan plan_split(const AttnArgs& a) {
+  SplitPlan p{0, 0, 0, 0};
+  const bool pipe = (a.D == 64 || a.D == 128) &&
+                    (a.kernel == 1 || (a.kernel == 0 && a.D == 128 && a.Sk >= kOneTileMinKeys));
+  if (!pipe || a.win_ct > 0 || a.causal || a.causal_b) return p;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return p;
+  const int64_t units = static_cast<int64_t>((a.Sq + kBlockM - 1) / kBlockM) * a.Hq * a.B;
+  const int64_t r = units % sms;
+  if (r == 0) return p;
+  const int64_t n_max = (a.Sk + kBlockN - 1) / kBlockN;
+  const int64_t pieces = min(static_cast<int64_t>(sms) / r, max(int64_t{1}, n_max / 2));
+  if (pieces < 2) return p;
+  p.full = static_cast<int>(units - r);
+  p.tail = static_cast<int>(r);
+  p.pieces = static_cast<int>(pieces);
+  p.bytes = static_cast<size_t>(r) * pieces * kBlockM * (a.D + 2) * sizeof(float);
+  return p;
+}
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   // Kernels (measured on GB300 with the workloads' shapes):
   //   1  one 128-row query tile per CTA, Q in tensor memory, two MMA-issuing
@@ -626,6 +655,11 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   //   3  the persistent kernel (one CTA per SM over all units), on request.
   // a.kernel: 0 = by shape, else the kernel above (head dims it lacks fall
   // back to the shape rule's next choice).
+  if (a.split_pieces > 0) {  // planned by plan_split: the one-query-tile kernel
+    if (a.D == 64) return launch_pipe<64, 12>(a, stream);
+    if (a.D == 128) return launch_pipe<128, 7>(a, stream);
+    return cudaErrorInvalidValue;
+  }
   if (a.kernel == 3 && a.win_ct == 0) {
     if (a.D == 64) return launch_persist<64, 12>(a, stream);
     if (a.D == 128) return launch_persist<128, 7>(a, stream);

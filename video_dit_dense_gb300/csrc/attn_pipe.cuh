@@ -56,9 +56,15 @@ struct PipeCfg {
 
 // WIN: chunked-window tile lists and masking (a.win_ct > 0); the dense
 // instantiation carries none of that code.
-template <int D, int NSTAGE, bool WIN>
+// SPLIT: the split-key tail (dense only; 1-D grid).  CTAs [0, split_full)
+// are whole units, taken in the order of the 3-D grid (query block fastest,
+// then head, then batch item); CTA split_full + i computes key-range piece
+// i % split_pieces of unit split_full + i / split_pieces and writes its
+// partial (unnormalised O, running max, row sum) to slot i of split_ws.
+template <int D, int NSTAGE, bool WIN, bool SPLIT = false>
 __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant__ AttnArgs a) {
   using C = PipeCfg<D, NSTAGE>;
+  static_assert(!(WIN && SPLIT), "the split tail is for dense attention");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -86,13 +92,27 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   const int lane = threadIdx.x & 31;
 
   // ---- work unit: (b, h, 128-row query tile) -------------------------------
-  const int b = blockIdx.z;
-  const int h = blockIdx.y;
+  int ux = static_cast<int>(blockIdx.x), uy = static_cast<int>(blockIdx.y), uz = static_cast<int>(blockIdx.z);
+  int piece = -1;  // split tail: this CTA's key-range piece of its unit
+  const int nqb = SPLIT ? (a.Sq + kBlockM - 1) / kBlockM : static_cast<int>(gridDim.x);
+  if constexpr (SPLIT) {
+    int unit = static_cast<int>(blockIdx.x);
+    if (unit >= a.split_full) {
+      const int i = unit - a.split_full;
+      unit = a.split_full + i / a.split_pieces;
+      piece = i % a.split_pieces;
+    }
+    ux = unit % nqb;
+    uy = (unit / nqb) % a.Hq;
+    uz = unit / (nqb * a.Hq);
+  }
+  const int b = uz;
+  const int h = uy;
   const int kvh = h / (a.Hq / a.Hkv);
   // Longest units first: with a causal mask the last query blocks; under the
   // chunked window the first ones (blocks holding anchor rows see every key,
   // and the last chunk's window is cut at the sequence end).
-  const int qb = WIN ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
+  const int qb = WIN ? ux : nqb - 1 - ux;
   const int q0 = qb * kBlockM;
   int kv_lim = a.Sk;
   if (a.kv_len) kv_lim = min(kv_lim, max(a.kv_len[b], 0));
@@ -131,6 +151,14 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       }
     }
   }
+  int tile_lo = 0;  // first key tile of the CTA's range (a split piece's share of its unit)
+  if constexpr (SPLIT) {
+    if (piece >= 0) {
+      const int lo = piece * n_tiles / a.split_pieces, hi = (piece + 1) * n_tiles / a.split_pieces;
+      tile_lo = lo;
+      n_tiles = hi - lo;
+    }
+  }
   // Load order = consumption order: K_0, K_1, K_2, then K_{j+3} (if any) and
   // V_j for j = 0, 1, ...  Load index of V_j: the K loads up to
   // K_{min(j+3, n-1)} and the V loads before it; K_j (j >= 3) sits right
@@ -145,13 +173,13 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   // query block spreads the CTAs that run at the same time (neighbouring
   // query blocks of one head) over different K/V tiles instead of having all
   // of them read the same tile's lines at once.
-  const int rot = n_tiles > 0 ? static_cast<int>(blockIdx.x) % n_tiles : 0;
-  auto tile_of = [rot, n_lead, mid0, n_tiles](int j) {
+  const int rot = n_tiles > 0 ? ux % n_tiles : 0;
+  auto tile_of = [rot, n_lead, mid0, n_tiles, tile_lo](int j) {
     const int m = j + rot < n_tiles ? j + rot : j + rot - n_tiles;  // position in the CTA's tile list
     if constexpr (WIN) {
       return m < n_lead ? m : mid0 + (m - n_lead);
     } else {
-      return m;
+      return tile_lo + m;
     }
   };
   // Tile j's barriers of parity j % 2 complete for the (j / 2)-th time.
@@ -167,7 +195,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       if (tb < n_lead) m = tb;
       else if (tb >= mid0 && tb < mid0 + n_tiles - n_lead) m = n_lead + (tb - mid0);
     } else {
-      if (tb < n_tiles) m = tb;
+      if (tb >= tile_lo && tb < tile_lo + n_tiles) m = tb - tile_lo;
     }
     if (m >= 0) j_pad = m >= rot ? m - rot : m - rot + n_tiles;
   }
@@ -483,7 +511,30 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       ok = __all_sync(0xFFFFFFFFu, wait_pv(n_tiles - 1));
       tc_fence_after();
     }
-    if (ok) {
+    if (SPLIT && ok && piece >= 0) {
+      // Partial of this key range: unnormalised O, the running max in scaled
+      // log2 units (-inf when no key of the range was allowed) and the row
+      // sum; the combine kernel weighs the pieces by 2^(m - max m).
+      float* part = a.split_ws + static_cast<size_t>(static_cast<int>(blockIdx.x) - a.split_full) * (kBlockM * (D + 2));
+      float4* prow = reinterpret_cast<float4*>(part + t * D);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          prow[c * 8 + v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                        __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+      }
+      part[kBlockM * D + t] = m_ref;
+      part[kBlockM * D + kBlockM + t] = l;
+    } else if (ok) {
       const bool live_row = row < a.Sq;
       const bool zero_row = row >= q_lim || n_tiles == 0 || !(l > 0.0f);
       const float inv = zero_row ? 0.0f : 1.0f / l;
@@ -518,9 +569,91 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   }
 }
 
+// Output rows of the split tail's units from their pieces' partials:
+// M = max_p m_p, o = (sum_p 2^(m_p - M) O_p) / (sum_p 2^(m_p - M) l_p),
+// rounded once to bf16; rows past q_len and rows with no allowed key are
+// zeros.  One warp per output row: lanes read the pieces' (m, l) side by side
+// (lane i takes pieces i, i + 32, ...; max and sum by a fixed butterfly), then
+// every lane accumulates its D/32 channels over the pieces in order, with the
+// loads of several pieces in flight.  Deterministic: a fixed order throughout.
+template <int D>
+__global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constant__ AttnArgs a) {
+  constexpr int V = D / 32;
+  const int gw = static_cast<int>((blockIdx.x * 256u + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= a.split_tail * kBlockM) return;  // warp-uniform
+  const int tu = gw / kBlockM, t = gw % kBlockM;
+  const int nqb = (a.Sq + kBlockM - 1) / kBlockM;
+  const int unit = a.split_full + tu;
+  const int ux = unit % nqb, h = (unit / nqb) % a.Hq, b = unit / (nqb * a.Hq);
+  const int row = (nqb - 1 - ux) * kBlockM + t;
+  if (row >= a.Sq) return;  // warp-uniform
+  int q_lim = a.Sq;
+  if (a.q_len) q_lim = min(q_lim, max(a.q_len[b], 0));
+  const int P = a.split_pieces;
+  const size_t stride = static_cast<size_t>(kBlockM) * (D + 2);
+  const float* part0 = a.split_ws + static_cast<size_t>(tu) * P * stride;
+  float M = -INFINITY;
+  for (int p = lane; p < P; p += 32) M = fmaxf(M, part0[p * stride + kBlockM * D + t]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  float L = 0.0f, acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+  if (M != -INFINITY) {
+    for (int p0 = 0; p0 < P; p0 += 32) {
+      const int p = p0 + lane;
+      float w = 0.0f, lw = 0.0f;
+      if (p < P) {
+        w = exp2f(part0[p * stride + kBlockM * D + t] - M);  // a piece with m = -inf weighs 0
+        lw = w * part0[p * stride + kBlockM * D + kBlockM + t];
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) lw += __shfl_xor_sync(0xFFFFFFFFu, lw, off);
+      L += lw;
+      const int n = min(32, P - p0);
+      const float* orow = part0 + static_cast<size_t>(p0) * stride + t * D + lane * V;
+#pragma unroll 8
+      for (int i = 0; i < n; ++i) {
+        const float wi = __shfl_sync(0xFFFFFFFFu, w, i);
+        float x[V];
+        if constexpr (V == 4) {
+          const float4 f = __ldg(reinterpret_cast<const float4*>(orow + i * stride));
+          x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+        } else {
+          const float2 f = __ldg(reinterpret_cast<const float2*>(orow + i * stride));
+          x[0] = f.x; x[1] = f.y;
+        }
+#pragma unroll
+        for (int c = 0; c < V; ++c) acc[c] = fmaf(wi, x[c], acc[c]);
+      }
+    }
+  }
+  const bool zero = row >= q_lim || !(L > 0.0f);
+  const float inv = zero ? 0.0f : 1.0f / L;
+  uint16_t* dst = a.o + ((static_cast<int64_t>(b) * a.Sq + row) * a.Hq + h) * D + lane * V;
+  if constexpr (V == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+}
+
 template <int D, int NSTAGE>
 cudaError_t launch_pipe(const AttnArgs& a, cudaStream_t stream) {
   using C = PipeCfg<D, NSTAGE>;
+  if (a.split_pieces > 0) {
+    auto kern = attn_pipe_kernel<D, NSTAGE, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int ctas = a.split_full + a.split_tail * a.split_pieces;
+    kern<<<ctas, C::kThreads, C::kSmemBytes, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int warps = a.split_tail * kBlockM;
+    split_combine_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
   auto kern = a.win_ct > 0 ? attn_pipe_kernel<D, NSTAGE, true> : attn_pipe_kernel<D, NSTAGE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -93,7 +93,20 @@ struct AttnArgs {
   // chunked window (self-attention, one-query-tile kernel only): tokens per
   // chunk (0 = dense), anchor tokens, radius in chunks
   int win_ct, win_af, win_r;
+  // Split-key tail (one-query-tile kernel, dense): the first split_full work
+  // units run whole; each of the remaining split_tail units is cut into
+  // split_pieces key ranges whose partial (O, m, l) go to split_ws, and a
+  // combine kernel writes their output rows.  split_pieces == 0: no split.
+  int split_full, split_tail, split_pieces;
+  float* split_ws;
 };
+// Plan of the split-key tail for a prefill call on the current device (all
+// zero when the call runs without it) and the workspace bytes it needs.
+struct SplitPlan {
+  int full, tail, pieces;
+  size_t bytes;
+};
+SplitPlan plan_split(const AttnArgs& a);
 // Key length from which the one-query-tile kernel is chosen (head_dim 64/128).
 constexpr int kOneTileMinKeys = 1024;
 // Box rows of the Q/K/V maps built by the launcher.
