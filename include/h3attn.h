@@ -213,6 +213,38 @@ h3attn_status_t h3attn_prefill_workspace_size(int B, int Sq, int Sk, int Hq, int
                                               const h3attn_mask_t* mask, int causal, size_t* bytes);
 
 /*
+ * Dense prefill attention that allocates nothing, for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this call; it
+ * exists for hosts that must not call cudaMalloc (or let a library do so):
+ * runtimes and plugin interfaces that own every device allocation and plan
+ * memory ahead of time, inference servers that keep allocation (which can
+ * synchronise the device) off the serving path, and code running while a
+ * stream is being captured, where an allocation would fail.  It computes
+ * what h3attn_prefill_ws() computes with a workspace, but the split-key
+ * tail's scratch is a fixed 12 MiB array inside the library's device code
+ * instead of caller memory.  Every device that loads the library holds that
+ * array until the process exits, whether or not this call is used.
+ *
+ * The caller still passes q, k, v and o; arguments, layout and errors as for
+ * h3attn_prefill().  A call whose tail would need more than 12 MiB of scratch
+ * (h3attn_prefill_workspace_size() above 12582912 bytes; at most 10.1 MB at
+ * head dim 128 on 152 SMs) is rejected with H3ATTN_ERR_INVALID_ARG before
+ * anything is launched.  Calls that need no scratch run exactly as
+ * h3attn_prefill().
+ * The first call on each device looks up the array's device address (and may
+ * load the library's device code on that device); make that first call
+ * before any stream capture.
+ * All calls on a device share the one array, and it keeps the last call's
+ * partial results: each call overwrites every slot it reads, so nothing needs
+ * clearing, but calls whose kernels can overlap on the GPU (different streams,
+ * or host threads racing on one stream) race on the array and must be
+ * ordered by the caller.
+ */
+h3attn_status_t h3attn_prefill_noalloc(const void* q, const void* k, const void* v, void* o, int B, int Sq,
+                                       int Sk, int Hq, int Hkv, int D, float scale,
+                                       const h3attn_mask_t* mask, int causal, h3attn_stream_t stream);
+
+/*
  * Fused RMSNorm -> indexed AdaLN scale/shift modulation of DiT hidden rows
  * (TeleFuser PR #37 "perf(minimax-h3): optimize Ulysses attention and DiT
  * kernels", section 2.5: "RMSNorm -> indexed scale/shift modulation" in one

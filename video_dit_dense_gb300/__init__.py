@@ -48,7 +48,8 @@ H3ATTN_ERR_TIMEOUT = 7
 
 # Every symbol include/h3attn.h declares.
 EXPORTED = ("h3attn_qk_norm_rope", "h3attn_qk_norm_rope_out", "h3attn_prefill", "h3attn_prefill_ws",
-            "h3attn_prefill_workspace_size", "h3attn_prefill_window", "h3attn_rmsnorm_modulate",
+            "h3attn_prefill_workspace_size", "h3attn_prefill_noalloc", "h3attn_prefill_window",
+            "h3attn_rmsnorm_modulate",
             "h3attn_status_string", "h3attn_check_device_status", "h3attn_version")
 
 
@@ -103,6 +104,9 @@ def load(path: str = LIB_PATH):
             lib.h3attn_prefill_workspace_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(h3attn_mask_t), I,
                                                           ctypes.POINTER(ctypes.c_size_t)]
             lib.h3attn_prefill_workspace_size.restype = I
+            lib.h3attn_prefill_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, F,
+                                                   ctypes.POINTER(h3attn_mask_t), I, P]
+            lib.h3attn_prefill_noalloc.restype = I
             lib.h3attn_prefill_window.argtypes = [P, P, P, P, I, I, I, I, I, F, ctypes.POINTER(h3attn_window_t),
                                                   ctypes.POINTER(h3attn_mask_t), P]
             lib.h3attn_prefill_window.restype = I
@@ -280,6 +284,35 @@ def h3attn_prefill_workspace_size(B, Sq, Sk, Hq, Hkv, D, mask: Mask | None = Non
     st = _lib.h3attn_prefill_workspace_size(B, Sq, Sk, Hq, Hkv, D, mptr, int(bool(causal)), ctypes.byref(out))
     _raise_if(st, "h3attn_prefill_workspace_size")
     return int(out.value)
+
+
+# Bytes of the fixed scratch array behind h3attn_prefill_noalloc.
+NOALLOC_SCRATCH_BYTES = 12 << 20
+
+
+def h3attn_prefill_noalloc(q, k, v, o, scale=None, mask: Mask | None = None, causal=False, stream=None):
+    """h3attn_prefill with the split-key tail's scratch in the library's fixed
+    12 MiB device array: the call allocates nothing (for hosts that cannot
+    allocate device memory).  Calls whose kernels may overlap must be ordered
+    by the caller, since they share the array."""
+    load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_bf16(name, t)
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or tuple(o.shape) != tuple(q.shape):
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, "shape mismatch between q, k, v and o")
+    if scale is None:
+        scale = 1.0 / float(D) ** 0.5
+    mptr = None if mask is None else _mask_struct(mask, B)
+    need = h3attn_prefill_workspace_size(B, Sq, Sk, Hq, Hkv, D, mask, causal)
+    if need > NOALLOC_SCRATCH_BYTES:
+        raise H3AttnError(H3ATTN_ERR_INVALID_ARG, f"h3attn_prefill_noalloc: this call needs {need} bytes of "
+                                                  f"scratch, more than the fixed {NOALLOC_SCRATCH_BYTES}")
+    st = _lib.h3attn_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Sq, Sk, Hq, Hkv, D, float(scale), mptr,
+                                     int(bool(causal)), _stream_handle(stream))
+    _raise_if(st, "h3attn_prefill_noalloc")
+    return o
 
 
 def prefill_workspace(q, k, mask: Mask | None = None, causal=False):

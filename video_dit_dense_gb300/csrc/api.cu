@@ -318,6 +318,59 @@ h3attn_status_t h3attn_prefill_ws(const void* q, const void* k, const void* v, v
                  stream);
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Prefill for callers that cannot allocate device memory (h3attn_prefill_noalloc).
+// The split-key tail's partials go to one fixed array that the library's
+// device code owns; it exists on every device that loads the library, from
+// the moment the device code is loaded until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t{12} << 20;  // 12 MiB: 152 SMs x 128 rows x 130 floats fit
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+// Device address of the array on each device.  In host code the array's name
+// is only a stand-in that the runtime maps to the device copy, so a kernel
+// must be given the address cudaGetSymbolAddress returns for the current
+// device, never the name itself.  Looked up on the first call on a device.
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+h3attn_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return H3ATTN_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return H3ATTN_ERR_UNSUPPORTED_DEVICE;
+  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return H3ATTN_ERR_LAUNCH;
+    g_noalloc_addr[dev].store(p, std::memory_order_release);  // racing first calls store the same address
+  }
+  *out = p;
+  return H3ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+h3attn_status_t h3attn_prefill_noalloc(const void* q, const void* k, const void* v, void* o, int B, int Sq,
+                                       int Sk, int Hq, int Hkv, int D, float scale, const h3attn_mask_t* mask,
+                                       int causal, h3attn_stream_t stream) {
+  size_t need = 0;
+  h3attn_status_t st = h3attn_prefill_workspace_size(B, Sq, Sk, Hq, Hkv, D, mask, causal, &need);
+  if (st != H3ATTN_OK) return st;
+  if (need > kNoAllocScratchBytes) return H3ATTN_ERR_INVALID_ARG;  // more scratch than the fixed array holds
+  void* scratch = nullptr;
+  if (need > 0) {
+    st = noalloc_scratch(&scratch);
+    if (st != H3ATTN_OK) return st;
+  }
+  // Every slot the combine reads is written by this call's pieces in full, so
+  // nothing left in the array by an earlier call needs clearing.
+  return prefill(q, k, v, o, B, Sq, Sk, Hq, Hkv, D, scale, mask, causal, nullptr, scratch, kNoAllocScratchBytes,
+                 stream);
+}
+
 h3attn_status_t h3attn_prefill_window(const void* q, const void* k, const void* v, void* o, int B, int S,
                                       int Hq, int Hkv, int D, float scale, const h3attn_window_t* win,
                                       const h3attn_mask_t* mask, h3attn_stream_t stream) {
