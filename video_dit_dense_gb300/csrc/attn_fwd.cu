@@ -191,7 +191,7 @@ __device__ __forceinline__ void zero_padding_rows(uint32_t tile, int r0, int lan
 constexpr int kTraceTiles = 512;
 enum TraceEv {
   kEvProdK, kEvProdV, kEvMmaK, kEvMmaQK0, kEvMmaQK1, kEvMmaV, kEvMmaPV0, kEvMmaPV1,
-  kEvSmS0, kEvSmLd0, kEvSmExp0, kEvSmArr0, kEvSmS1, kEvSmLd1, kEvSmExp1, kEvSmArr1, kNumEv
+  kEvSmS0, kEvSmLd0, kEvSmExp0, kEvSmArr0, kEvSmS1, kEvSmLd1, kEvSmExp1, kEvSmArr1, kEvCtaStart, kEvCtaEnd, kNumEv
 };
 __device__ unsigned long long g_trace[kNumEv][kTraceTiles];
 #define H3_TRACE(ev, j)                                                                     \

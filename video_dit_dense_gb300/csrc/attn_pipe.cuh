@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) H3_TRACE(kEvCtaStart, 0);
 
   // ---- work unit: (b, h, 128-row query tile) -------------------------------
   int ux = static_cast<int>(blockIdx.x), uy = static_cast<int>(blockIdx.y), uz = static_cast<int>(blockIdx.z);
@@ -561,6 +562,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
     }
   }
 
+  if (threadIdx.x == 0) H3_TRACE(kEvCtaEnd, 0);
   tc_fence_before();
   __syncthreads();
   if (warp == C::kMmaWarp) {
