@@ -558,15 +558,22 @@ def cpu_baseline(wl, inp, seconds):
     import numpy as np
 
     import oracle
-    cores = os.cpu_count() or 1
+    cores = min(os.cpu_count() or 1, 64)  # the oracle's thread count (one per core, at most 64)
     rng = np.random.default_rng(0)
-    # norm/RoPE oracle (fp64) on the q and k of one slice of tokens
-    t0 = time.perf_counter()
-    n_tok = min(wl.Sq, 2048)
-    oracle.qk_norm_rope_f64(np.ascontiguousarray(inp.q[:, :n_tok]), inp.wq, inp.cos, inp.sin, wl.rotary_dim, wl.eps)
-    t_norm = time.perf_counter() - t0
+    # norm/RoPE oracle (fp64) on consecutive token slices of q, then k, for at least a second
+    norm_rows, t_norm, tok = 0, 0.0, 0
+    while t_norm < 1.0 and wl.norm_rope:
+        src = inp.q if (tok // wl.Sq) % 2 == 0 else inp.k
+        t_lo = tok % wl.Sq
+        n_tok = min(4096, wl.Sq - t_lo)
+        x = np.ascontiguousarray(src[:, t_lo:t_lo + n_tok])
+        t0 = time.perf_counter()
+        oracle.qk_norm_rope_f64(x, inp.wq, inp.cos[t_lo:], inp.sin[t_lo:], wl.rotary_dim, wl.eps)
+        t_norm += time.perf_counter() - t0
+        norm_rows += x.shape[0] * x.shape[1] * x.shape[2]
+        tok += n_tok
     # attention oracle on sampled rows, growing the sample until ~`seconds`
-    n = 8
+    n = min(8, wl.B * wl.Sq * wl.Hq)
     done_rows, t_att = 0, 0.0
     while t_att < seconds:
         ids = np.sort(rng.choice(wl.B * wl.Sq * wl.Hq, size=n, replace=False)).astype(np.int64)
@@ -574,13 +581,16 @@ def cpu_baseline(wl, inp, seconds):
         oracle.attention_f64(inp.q, inp.k, inp.v, wl.scale, row_ids=ids)
         t_att += time.perf_counter() - t0
         done_rows += n
-        n = min(n * 2, 4096)
+        n = min(n * 2, 4096, wl.B * wl.Sq * wl.Hq)
     flops_per_row = 4.0 * wl.Sk * wl.D
+    total_rows = wl.B * wl.Sq * wl.Hq
     return {"value": round(done_rows * flops_per_row / t_att / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{done_rows} attention rows of {wl.name} (fp64, all {wl.Sk} keys each) in {t_att:.1f} s; "
-                      f"norm/RoPE fp64 on {n_tok * wl.Hq} q rows in {t_norm:.2f} s",
-            "norm_rope_gbs": round(2.0 * n_tok * wl.Hq * wl.D * 2 / t_norm / 1e9, 3)}
+            "sample": f"attention rate extrapolated from {done_rows} sampled row evaluations ({wl.name} has "
+                      f"{total_rows} output rows; fp64, all {wl.Sk} keys each, {t_att:.1f} s; the full step would "
+                      f"take ~{total_rows / done_rows * t_att:.0f} s); norm/RoPE fp64 on {norm_rows} q/k rows "
+                      f"in {t_norm:.2f} s",
+            "norm_rope_gbs": round(norm_rows * wl.D * 2 * 2 / t_norm / 1e9, 3) if norm_rows else None}
 
 
 def run_reference(args):
