@@ -501,7 +501,7 @@ ONE_TILE_MIN_KEYS = 1024
 def _attn_kernel_name(wl):
     sel = os.environ.get("H3ATTN_ATTN_KERNEL", "")
     if wl.D == 256:
-        return "attn_fwd_kernel<256,1,2,1>"
+        return "attn_fwd_kernel<256,1,2,1>" if sel in ("2", "3", "4") else "attn_wide_kernel<5>"
     if sel == "3":
         return {64: "attn_persist_kernel<64,12>", 128: "attn_persist_kernel<128,7>"}[wl.D]
     one_tile = sel == "1" or (sel not in ("2", "4") and wl.D == 128 and wl.Sk >= ONE_TILE_MIN_KEYS)

@@ -44,9 +44,10 @@ def full_case(h3, B, Sq, Sk, Hq, Hkv, D, seed=0, causal=False, kv_len=None, q_le
 # Every edge case runs on every attention kernel: "1" = one query tile per CTA
 # (Q in tensor memory), "2" = two query tiles per CTA, "3" = the persistent
 # kernel (one CTA per SM over all units), "4" = one query tile per CTA, two
-# CTAs per SM (head_dim 256 falls back to "2" for "3" and "4").  Without the
-# override the library picks by key length.
-@pytest.fixture(params=["1", "2", "3", "4"], ids=["one_tile", "two_tiles", "persistent", "two_ctas"])
+# CTAs per SM (head_dim 256 falls back to "2" for "3" and "4"), "5" = the
+# head-dim-256 kernel with double-buffered scores (other head dims take the
+# library's choice).  Without the override the library picks by shape.
+@pytest.fixture(params=["1", "2", "3", "4", "5"], ids=["one_tile", "two_tiles", "persistent", "two_ctas", "wide"])
 def kernel(request, monkeypatch):
     monkeypatch.setenv("H3ATTN_ATTN_KERNEL", request.param)
     return request.param

@@ -184,10 +184,10 @@ h3attn_status_t h3attn_qk_norm_rope_out(const void* q, const void* k, void* q_ou
 
 namespace {
 
-// Kernel choice override (tests run every case on every kernel): "1" .. "4".
+// Kernel choice override (tests run every case on every kernel): "1" .. "5".
 int kernel_override() {
   const char* kern = getenv("H3ATTN_ATTN_KERNEL");
-  return (kern && kern[0] >= '1' && kern[0] <= '4') ? kern[0] - '0' : 0;
+  return (kern && kern[0] >= '1' && kern[0] <= '5') ? kern[0] - '0' : 0;
 }
 
 // The fields of AttnArgs that decide the kernel and the split-key plan.

@@ -558,6 +558,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
 
 #include "attn_pipe.cuh"
 #include "attn_persist.cuh"
+#include "attn_wide.cuh"
 
 template <int D, int NQ, int NSTAGE, int CTAS = 1>
 cudaError_t launch_cfg(const AttnArgs& a, cudaStream_t stream) {
@@ -650,8 +651,10 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   //   4  the two-tile kernel's code with one query tile per CTA, a short ring
   //      and two CTAs per SM (one CTA's prologue and epilogue overlap the
   //      other's products): head_dim 128 below 1024 keys, head_dim 64;
-  //   2  two query tiles per CTA sharing each K/V tile: head_dim 256 (one
-  //      tile per CTA there), otherwise only on request;
+  //   5  head_dim 256: one query tile per CTA with double-buffered scores
+  //      (P over its score buffer, Q and half-tiles of K/V in shared memory);
+  //   2  two query tiles per CTA sharing each K/V tile (head_dim 256: one
+  //      tile with a single score buffer), only on request;
   //   3  the persistent kernel (one CTA per SM over all units), on request.
   // a.kernel: 0 = by shape, else the kernel above (head dims it lacks fall
   // back to the shape rule's next choice).
@@ -659,6 +662,11 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     if (a.D == 64) return launch_pipe<64, 12>(a, stream);
     if (a.D == 128) return launch_pipe<128, 7>(a, stream);
     return cudaErrorInvalidValue;
+  }
+  if (a.kernel == 5 && a.D != 256) {  // head dims without a wide kernel: the shape rule below
+    AttnArgs b = a;
+    b.kernel = 0;
+    return launch_attention(b, stream);
   }
   if (a.kernel == 3 && a.win_ct == 0) {
     if (a.D == 64) return launch_persist<64, 12>(a, stream);
@@ -673,7 +681,9 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     case 128:
       return one_tile ? launch_pipe<128, 7>(a, stream)
                       : (two_ctas ? launch_cfg<128, 1, 2, 2>(a, stream) : launch_cfg<128, 2, 4>(a, stream));
-    case 256: return launch_cfg<256, 1, 2>(a, stream);
+    case 256:  // double-buffered scores; the two-tile kernel's code on request ("2", and "3"/"4" fall back to it)
+      return (a.kernel == 0 || a.kernel == 1 || a.kernel == 5) ? launch_wide<5>(a, stream)
+                                                               : launch_cfg<256, 1, 2>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
