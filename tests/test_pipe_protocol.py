@@ -28,7 +28,12 @@ Without the flag the phase wait could pass on an older fill of the stage.
 run_two_tile models the two-tile kernel (one MMA-issuing thread, NQ query
 tiles sharing each K/V tile, P_q written over S_q): the issuer's wait for
 O_q += P_q V before the next S_q is what keeps S_q from overwriting an unread
-P_q, since the two products write different accumulators."""
+P_q, since the two products write different accumulators.
+
+run_wide models the head-dim-256 kernel (two score buffers, P over its
+buffer, K/V in half tiles, O in two halves): besides the checks above, it
+shows that its epilogue needs the one-shot drain wait, because a parity wait
+on the last product can pass while the product before it is still pending."""
 import random
 
 import pytest
@@ -451,4 +456,195 @@ def test_two_tile_kernel_protocol_is_clean(NQ, nstage):
 
 def test_two_tile_kernel_needs_the_wait_before_the_next_score_product():
     bad = sum(bool(run_two_tile(8, 2, 4, trial, wait_pv_before_s=False)) for trial in range(300))
+    assert bad > 0
+
+
+def run_wide(n_tiles, nstage, seed, pad_tile=None, epilogue="drain"):
+    """One random interleaving of the head-dim-256 kernel (attn_wide): score
+    buffers S_0, S_1 (tile j in S_{j mod 2}, P_j written over it), O in two
+    128-channel halves, Q loaded once; the producer fills an nstage ring of
+    half tiles in the order K_0, K_1, then V_j, K_{j+2} (two halves each);
+    one MMA thread issues S_0 = Q K_0^T and S_1 = Q K_1^T, then per tile j
+    waits for P_j, issues O_h += P_j V_j[h] for h = 0, 1, commits pv_done,
+    and (if j + 2 < n) waits for that product before S_{j mod 2} =
+    Q K_{j+2}^T; the softmax waits for S_j, may rescale O (after waiting for
+    the previous product), writes P_j over S_j and publishes it.  The
+    epilogue waits for the MMA thread's one-shot drain commit ("drain") or, as
+    a parity wait on pv_done for the last tile ("parity"), which two pending
+    products can alias.  Returns the list of protocol violations."""
+    rng = random.Random(seed)
+    q_full, drain, v_clean = Bar(), Bar(), Bar()
+    kv_full = [Bar() for _ in range(nstage)]
+    kv_empty = [Bar() for _ in range(nstage)]
+    s_full, p_ready = [Bar(), Bar()], [Bar(), Bar()]
+    pv_done = Bar()
+    st = {"Q": False, "stage": [None] * nstage, "S": [None, None], "P": [None, None], "O": [0, 0],
+          "pad_issued": False, "zeroed": None}
+    queue, copies, errors = [], [], []
+    n_lead = min(n_tiles, 2)
+
+    def ld_v(j):
+        return 2 * n_lead + 2 * j + 2 * max(0, min(j, n_tiles - 2))
+
+    def ld_k(j):
+        return 2 * j if j < 2 else ld_v(j - 2) + 2
+
+    def producer():
+        copies.append(("Q", None))
+        order = [("K", j, h) for j in range(n_lead) for h in (0, 1)]
+        for j in range(n_tiles):
+            order += [("V", j, 0), ("V", j, 1)]
+            if j + 2 < n_tiles:
+                order += [("K", j + 2, 0), ("K", j + 2, 1)]
+        for pos, what in enumerate(order):
+            assert pos == (ld_k(what[1]) if what[0] == "K" else ld_v(what[1])) + what[2]
+            sidx, ph = pos % nstage, (pos // nstage) & 1
+            yield lambda sidx=sidx, ph=ph: kv_empty[sidx].ok(ph ^ 1)
+            copies.append((sidx, what))
+            if what == ("V", pad_tile, 1):
+                st["pad_issued"] = True
+
+    def pad_warp():
+        p0 = ld_v(pad_tile)
+        yield lambda: st["pad_issued"]
+        for pos in (p0, p0 + 1):
+            sidx, ph = pos % nstage, (pos // nstage) & 1
+            yield lambda sidx=sidx, ph=ph: kv_full[sidx].ok(ph)
+            if st["stage"][sidx] != ("V", pad_tile, pos - p0):
+                errors.append(f"padding warp zeroes stage {sidx} holding {st['stage'][sidx]}")
+        st["zeroed"] = pad_tile
+        v_clean.arrive()
+
+    def mma():
+        yield lambda: q_full.ok(0)
+
+        def issue_qk(j):
+            for h in (0, 1):
+                pos = ld_k(j) + h
+                sidx, ph = pos % nstage, (pos // nstage) & 1
+                yield lambda sidx=sidx, ph=ph: kv_full[sidx].ok(ph)
+                queue.extend([("qk", j, h, sidx, ("S", j & 1)), ("commit", kv_empty[sidx])])
+            queue.append(("commit", s_full[j & 1]))
+
+        for j in range(n_lead):
+            yield from issue_qk(j)
+        for j in range(n_tiles):
+            yield lambda j=j: p_ready[j & 1].ok((j >> 1) & 1)
+            if j == pad_tile:
+                yield lambda: v_clean.ok(0)
+            for h in (0, 1):
+                pos = ld_v(j) + h
+                sidx, ph = pos % nstage, (pos // nstage) & 1
+                yield lambda sidx=sidx, ph=ph: kv_full[sidx].ok(ph)
+                queue.extend([("pv", j, h, sidx, ("O", h)), ("commit", kv_empty[sidx])])
+            queue.append(("commit", pv_done))
+            if j + 2 < n_tiles:
+                yield lambda j=j: pv_done.ok(j & 1)
+                yield from issue_qk(j + 2)
+        queue.append(("commit", drain))
+
+    def softmax():
+        for j in range(n_tiles):
+            yield lambda j=j: s_full[j & 1].ok((j >> 1) & 1)
+            if st["S"][j & 1] != j:
+                errors.append(f"softmax reads S_{j & 1} holding {st['S'][j & 1]} for tile {j}")
+            if j > 0 and rng.random() < 0.5:   # the running max grew: rescale O
+                yield lambda j=j: pv_done.ok((j - 1) & 1)
+                if st["O"] != [j, j]:
+                    errors.append(f"softmax rescales O holding {st['O']} tiles at tile {j}")
+            st["P"][j & 1] = j
+            st["S"][j & 1] = None   # P is written over S
+            p_ready[j & 1].arrive()
+        if n_tiles:
+            if epilogue == "drain":
+                yield lambda: drain.ok(0)
+            else:
+                yield lambda: pv_done.ok((n_tiles - 1) & 1)
+            if st["O"] != [n_tiles, n_tiles]:
+                errors.append(f"epilogue reads O holding {st['O']} of {n_tiles} tiles")
+
+    partial_s = {}
+
+    def execute():
+        op = take_tensor_op(queue, rng)
+        if op[0] == "commit":
+            op[1].arrive()
+            return
+        kind, j, h, sidx, _ = op
+        if st["stage"][sidx] != (("K" if kind == "qk" else "V"), j, h):
+            errors.append(f"{kind} of tile {j} half {h} reads stage {sidx} holding {st['stage'][sidx]}")
+        if kind == "qk":
+            b = j & 1
+            if not st["Q"]:
+                errors.append(f"S of tile {j} reads Q before it landed")
+            if st["P"][b] is not None and min(st["O"]) <= st["P"][b]:
+                errors.append(f"S of tile {j} overwrites P of tile {st['P'][b]} before O += P V read it")
+            if h == 0:
+                partial_s[b] = j
+            elif partial_s.get(b) == j:
+                st["S"][b] = j
+                st["P"][b] = None
+        else:
+            if j == pad_tile and st["zeroed"] != j:
+                errors.append(f"P V of tile {j} reads V before its padding rows were zeroed")
+            if st["P"][j & 1] != j or st["O"][h] != j:
+                errors.append(f"O_{h} += P V of tile {j} reads P {st['P'][j & 1]} onto O of {st['O'][h]} tiles")
+            st["O"][h] = j + 1
+
+    roles = {"producer": producer(), "mma": mma(), "softmax": softmax()}
+    if pad_tile is not None:
+        roles["pad"] = pad_warp()
+    waits = {}
+    for name in list(roles):
+        try:
+            waits[name] = next(roles[name])
+        except StopIteration:
+            del roles[name]
+    while roles or queue or copies:
+        moves = [("role", r) for r in roles if waits[r]()]
+        if queue:
+            moves.append(("tensor", None))
+        moves += [("copy", i) for i in range(len(copies))]
+        if not moves:
+            return [f"deadlock: {sorted(roles)} waiting"]
+        kind, x = rng.choice(moves)
+        if kind == "role":
+            try:
+                waits[x] = roles[x].send(None)
+            except StopIteration:
+                del roles[x]
+        elif kind == "tensor":
+            execute()
+        else:
+            sidx, what = copies.pop(x)
+            if sidx == "Q":
+                st["Q"] = True
+                q_full.arrive()
+            else:
+                st["stage"][sidx] = what
+                kv_full[sidx].arrive()
+        if errors:
+            return errors
+    return errors
+
+
+@pytest.mark.parametrize("nstage", [2, 4, 5, 7])
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 17])
+def test_wide_pipeline_is_clean(n, nstage):
+    for trial in range(150):
+        assert run_wide(n, nstage, trial) == [], f"n {n}, nstage {nstage}, seed {trial}"
+
+
+@pytest.mark.parametrize("n", [1, 4, 16])
+def test_wide_padding_warp_zeroes_the_right_tile(n):
+    for trial in range(80):
+        for pad in sorted({0, n // 2, n - 1}):
+            assert run_wide(n, 5, trial, pad_tile=pad) == [], f"n {n}, pad {pad}, seed {trial}"
+
+
+def test_wide_parity_epilogue_can_read_o_early():
+    # with two score buffers the product of tile n - 2 may still be pending
+    # when P_{n-1} is stored, so a parity wait for the last product can pass
+    # on the completion of tile n - 3: the drain barrier is needed
+    bad = sum(bool(run_wide(n, 5, trial, epilogue="parity")) for n in (5, 8, 17) for trial in range(300))
     assert bad > 0
