@@ -95,3 +95,30 @@ def test_rmsnorm_modulate_past_2_to_the_31_elements(h3):
                                               np.ascontiguousarray(inp.idx[t0:t1]), 1e-6)
         got = y[t0:t1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
         np.testing.assert_array_equal(got, ref, err_msg=f"rows {t0}..{t1}")
+
+
+@pytest.mark.gpu
+def test_head_dim_256_attention_past_2_to_the_31_elements(h3):
+    """The head-dim-256 kernel (double-buffered scores) on a cross-attention
+    query of 2^31 + 8.5 M elements (4.3 GB): sampled rows on both sides of the
+    2^31-element line against the oracle, and the convex bound everywhere."""
+    import torch
+    D2, H2 = 256, 8
+    SQ2, SK2 = (1 << 20) + 4133, 128 + 77
+    line2 = (1 << 31) // (H2 * D2)
+    q = gen.normal_bshd(1, SQ2, H2, D2, 25, gen.STREAM_Q)
+    k = gen.normal_bshd(1, SK2, H2, D2, 25, gen.STREAM_K)
+    v = gen.normal_bshd(1, SK2, H2, D2, 25, gen.STREAM_V)
+    assert q.size > (1 << 31)
+    dq, dk, dv = to_dev(q), to_dev(k), to_dev(v)
+    do = torch.full_like(dq, float("nan"))
+    scale = 1.0 / np.sqrt(D2)
+    h3.h3attn_prefill(dq, dk, dv, do, scale)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    assert_convex_bound(dv, do, 1, "head dim 256 past 2^31 elements")
+    extra = (line2 - 1, line2, line2 + 1, SQ2 - 129, SQ2 - 128, SQ2 - 2)
+    ids = sample_rows(1, SQ2, H2, 16, seed=5, extra_rows=extra)
+    ref = oracle.attention_f64(q, k, v, scale, row_ids=ids)
+    got = do.view(-1, D2)[torch.from_numpy(ids).cuda()].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    check_close(got, ref, "head dim 256 cross past 2^31 elements")

@@ -91,6 +91,10 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) H3_TRACE(kEvCtaStart, 0);
+  // Split launch: the combine kernel, launched after this grid with
+  // programmatic stream serialization, may be scheduled as soon as every CTA
+  // of this grid has started; it waits for this grid's completion itself.
+  if constexpr (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- work unit: (b, h, 128-row query tile) -------------------------------
   int ux = static_cast<int>(blockIdx.x), uy = static_cast<int>(blockIdx.y), uz = static_cast<int>(blockIdx.z);
@@ -581,6 +585,10 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
 template <int D>
 __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int V = D / 32;
+  // Launched as a programmatic dependent of the split kernel: wait until that
+  // grid has completed and its partials are visible (a no-op when launched
+  // without the dependency).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gw = static_cast<int>((blockIdx.x * 256u + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= a.split_tail * kBlockM) return;  // warp-uniform
@@ -652,9 +660,20 @@ cudaError_t launch_pipe(const AttnArgs& a, cudaStream_t stream) {
     kern<<<ctas, C::kThreads, C::kSmemBytes, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // The combine as a programmatic dependent launch: its CTAs are placed
+    // while the split kernel's last pieces run and start the moment it ends.
     const int warps = a.split_tail * kBlockM;
-    split_combine_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((warps + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_combine_kernel<D>, a);
   }
   auto kern = a.win_ct > 0 ? attn_pipe_kernel<D, NSTAGE, true> : attn_pipe_kernel<D, NSTAGE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
