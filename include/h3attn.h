@@ -159,7 +159,8 @@ h3attn_status_t h3attn_qk_norm_rope_out(const void* q, const void* k, void* q_ou
  * Scheduling: a work unit is 128 query rows of one batch item and head; the
  * units are launched longest (causal) first and the hardware places them on
  * the SMs as they free up (one resident CTA per SM for head dim 128 from 1024
- * keys on, two otherwise).
+ * keys on and for head dim 256, two for head dim 64 and for head dim 128
+ * below 1024 keys).
  * Accumulation is float32 on the tensor cores; softmax in float32
  * with exp2; the output is rounded once to bf16.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_HEAD_DIM, UNSUPPORTED_DEVICE,
