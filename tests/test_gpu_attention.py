@@ -45,9 +45,12 @@ def full_case(h3, B, Sq, Sk, Hq, Hkv, D, seed=0, causal=False, kv_len=None, q_le
 # (Q in tensor memory), "2" = two query tiles per CTA, "3" = the persistent
 # kernel (one CTA per SM over all units), "4" = one query tile per CTA, two
 # CTAs per SM (head_dim 256 falls back to "2" for "3" and "4"), "5" = the
-# head-dim-256 kernel with double-buffered scores (other head dims take the
-# library's choice).  Without the override the library picks by shape.
-@pytest.fixture(params=["1", "2", "3", "4", "5"], ids=["one_tile", "two_tiles", "persistent", "two_ctas", "wide"])
+# head-dim-256 kernel with double-buffered scores, "6" = the head-dim-128
+# kernel that chains its work units, one CTA per SM (other head dims take the
+# library's choice for "5" and "6").  Without the override the library picks
+# by shape.
+@pytest.fixture(params=["1", "2", "3", "4", "5", "6"],
+                ids=["one_tile", "two_tiles", "persistent", "two_ctas", "wide", "chain"])
 def kernel(request, monkeypatch):
     monkeypatch.setenv("H3ATTN_ATTN_KERNEL", request.param)
     return request.param
@@ -194,15 +197,48 @@ def test_workload_sampled_rows(h3, name, seed):
 
 
 @pytest.mark.gpu
-def test_persistent_kernel_on_long_video(h3, monkeypatch):
-    """The software-persistent kernel (one CTA per SM walking the unit list)
-    at a full workload size: sampled rows against the oracle."""
-    monkeypatch.setenv("H3ATTN_ATTN_KERNEL", "3")
+@pytest.mark.parametrize("kern", ["3", "6"], ids=["persistent", "chain"])
+def test_persistent_kernel_on_long_video(h3, monkeypatch, kern):
+    """The kernels with one CTA per SM walking the unit list (the persistent
+    and the unit-chaining one) at a full workload size: sampled rows against
+    the oracle."""
+    monkeypatch.setenv("H3ATTN_ATTN_KERNEL", kern)
     wl, inp, q, k = _workload_inputs("long_video_h12", seed=42)
     got = _gpu_step(h3, wl, inp)
     ids = sample_rows(wl.B, wl.Sq, wl.Hq, 24, seed=43)
     ref = oracle.attention_f64(q, k, inp.v, wl.scale, row_ids=ids)
-    check_close(got.reshape(-1, wl.D)[ids], ref, "persistent long_video_h12")
+    check_close(got.reshape(-1, wl.D)[ids], ref, f"kernel {kern} long_video_h12")
+
+
+# The kernels with one CTA per SM take several units per CTA only when the
+# grid has several times more units than the GPU has SMs; the edge-case shapes
+# above give each CTA one unit at most.  These shapes give each 3 to 10, with
+# the unit changes the chaining kernel hands over between its warps: one- and
+# two-tile units, units with no key tile (rows past q_len), a padded tile in
+# every unit of a sample, cross-attention, per-sample causal masks, GQA and a
+# packed mask.
+@pytest.mark.gpu
+@pytest.mark.parametrize("kern", ["3", "6"], ids=["persistent", "chain"])
+def test_unit_walking_kernels_over_many_units(h3, monkeypatch, kern):
+    monkeypatch.setenv("H3ATTN_ATTN_KERNEL", kern)
+    full_case(h3, 4, 256, 256, 96, 96, 128, seed=31, causal=True, what=f"kernel {kern} short causal units")
+    B, Sq, Sk, Hq, Hkv, D = 2, 4096, 300, 24, 8, 128
+    kv_len = np.array([300, 173], np.int32)
+    q_len = np.array([4096, 1000], np.int32)
+    q = gen.normal_bshd(B, Sq, Hq, D, 32, gen.STREAM_Q)
+    k = gen.normal_bshd(B, Sk, Hkv, D, 32, gen.STREAM_K)
+    v = gen.normal_bshd(B, Sk, Hkv, D, 32, gen.STREAM_V)
+    scale = 1.0 / np.sqrt(D)
+    got = gpu_attention(h3, q, k, v, scale, kv_len=kv_len, q_len=q_len)
+    ids = sample_rows(B, Sq, Hq, 12, seed=33, extra_rows=(172, 173, 999, 1000, 1023, 1024, 2047, 2048))
+    ref = oracle.attention_f64(q, k, v, scale, False, kv_len, q_len, None, row_ids=np.asarray(ids, np.int64))
+    check_close(got.reshape(-1, D)[ids], ref, f"kernel {kern} cross-attention units")
+    assert not np.any(got[1, 1000:]), "rows past q_len are zeros"
+    full_case(h3, 2, 1024, 1024, 48, 16, 128, seed=35, kv_len=np.array([1024, 700], np.int32),
+              q_len=np.array([1024, 600], np.int32), causal_b=np.array([1, 0], np.uint8),
+              what=f"kernel {kern} per-sample causal units")
+    full_case(h3, 2, 1024, 1024, 32, 32, 128, seed=34, bits_density=0.5, kv_len=np.array([1024, 700], np.int32),
+              what=f"kernel {kern} packed mask units")
 
 
 def _structured_as_bits(B, Sq, Sk, kv_len, causal_b):

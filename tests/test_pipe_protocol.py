@@ -650,93 +650,74 @@ def test_wide_parity_epilogue_can_read_o_early():
     assert bad > 0
 
 
-def run_chain(units, nstage, seed, pad=None, chain_pv=True):
-    """One random interleaving of the unit-chaining kernel (attn_chain): one CTA
-    walks a list of work units (tile counts; 0 = a unit with nothing to
-    attend, whose rows the epilogue writes as zeros).  Units with tiles take
-    Q buffers and O accumulators by their rank kappa among such units: Q in
-    shared memory Q[kappa % 2], O in tensor memory O[kappa % 2].  Key tiles
-    of all units form one stream J; tile J's scores go to S[J % 2] and its P
-    over them.  Roles:
-      producer: Q_kappa (once the softmax released Q[kappa % 2]), then the
-        ring in the order K_0, K_1, then V_J, K_{J+2};
-      MMA thread p (tiles J = p mod 2): S[J%2] = Q K_J^T once its own previous
-        product on that buffer, P V of J - 2, has completed; then, once P_J is
-        published, V_J has landed, P V of J - 1 (the other thread) has
-        completed (both accumulate into one O) and, for a unit's first tile,
-        the epilogue has read that O buffer's previous unit: O += P V_J;
-        commit; the unit's last tile also commits o_full;
-      softmax: per tile waits for S_J, after a unit's last tile's scores
-        releases its Q buffer, may rescale O (after waiting for P V of J - 1),
-        writes P over S_J and publishes it; at a unit's end hands l to the
-        epilogue (once the epilogue read the buffer's previous unit);
-      epilogue: per unit with tiles waits for o_full and l, reads O, frees the
-        buffer;
-      pad (optional): for the tiles listed in `pad` zeroes V after the
-        producer's issued count covers it, and counts the tiles cleaned; the
-        tile's P V waits for that count.
-    chain_pv=False drops the cross-thread P V wait (planting the overlap it
-    guards against).  Returns the list of violations."""
+def run_chain(units, nstage, seed, pad=None, q_handoff="count", o_free_wait=True, q_free_wait=True):
+    """One random interleaving of the unit-chaining kernel (attn_chain): one
+    CTA walks a list of work units (tile counts; 0 = a unit with nothing to
+    attend, whose rows are written as zeros without any hand-off).  Units with
+    tiles are numbered kappa = 0, 1, ...; their key tiles form one stream J.
+    The per-tile protocol is the one-tile kernel's: two MMA threads, scores
+    three tiles ahead into S[J % 2], a single P buffer written once the
+    previous P V has completed.  At unit changes:
+      Q: the unit warps copy Q_kappa from a single shared-memory buffer
+        into the single tensor-memory Q buffer once the softmax has seen the
+        last score tile of unit kappa - 1 (its Q K^T are then complete), then
+        load Q_{kappa+1} into the shared buffer themselves (the producer,
+        which runs three tiles ahead over several short units, would have to
+        wait for that copy before its next K load: a cycle through the
+        epilogue, which waits for a P V whose V comes after that K), and
+        count the copy into q_ready; an MMA thread waits for q_ready > kappa
+        before its first Q K^T of unit kappa (q_handoff="parity": a phase
+        wait instead);
+      O: the MMA thread of a unit's last tile commits o_full after its P V;
+        the unit warps read O and the row sums (two slots) and free O; the
+        first P V of the next unit (no accumulate) waits for that.
+    pad: stream tiles whose V rows a padding warp zeroes (issued count, then
+    the stage's phase) before their P V.  o_free_wait / q_free_wait=False
+    drop those waits (planted mistakes).  Returns the list of violations."""
     rng = random.Random(seed)
-    tiles, first, last, kap = [], {}, {}, []  # stream tile -> (unit, j); unit -> first/last J
+    tiles, kap = [], []  # stream tile -> (unit, j, kappa); unit -> kappa or None
     kappa = 0
     for u, n in enumerate(units):
         kap.append(kappa if n else None)
-        for j in range(n):
-            if j == 0:
-                first[u] = len(tiles)
-            last[u] = len(tiles)
-            tiles.append((u, j))
+        tiles.extend((u, j, kappa) for j in range(n))
         kappa += bool(n)
     N = len(tiles)
     pad = set(pad or ())
     pad_order = sorted(pad)
     kv_full = [Bar() for _ in range(nstage)]
     kv_empty = [Bar() for _ in range(nstage)]
-    s_full, p_ready = [Bar(), Bar()], [Bar(), Bar()]
-    pv_done = [Bar(), Bar()]
-    q_full = [Bar(), Bar()]
-    q_free = [Bar(), Bar()]
-    o_full, o_free = [Bar(), Bar()], [Bar(), Bar()]
-    l_full = [Bar(), Bar()]
-    st = {"Q": [None, None], "S": [None, None], "P": [None, None], "O": [None, None], "O_read": [True, True],
-          "stage": [None] * nstage, "v_issued": 0, "cleaned": 0, "zeroed": set(), "l": [None, None]}
+    s_full, s_read = [Bar(), Bar()], [Bar(), Bar()]
+    p_ready, pv_done = [Bar(), Bar()], [Bar(), Bar()]
+    q_sfull, q_free, q_full = Bar(), Bar(), Bar()
+    o_full, o_free = Bar(), Bar()
+    l_full, l_free = [Bar(), Bar()], [Bar(), Bar()]
+    st = {"Qs": None, "Qt": None, "q_ready": 0, "S": [None, None], "P": None, "O": None, "O_read": True,
+          "l": [None, None], "stage": [None] * nstage, "v_issued": 0, "cleaned": 0, "zeroed": set()}
     queues = {0: [], 1: []}
     copies, errors = [], []
-    n_lead = min(N, 2)
 
     def ld_v(J):
-        return n_lead + J + max(0, min(J, N - 2))
+        return min(J + 4, N) + J
 
     def ld_k(J):
-        return J if J < 2 else ld_v(J - 2) + 1
+        return J if J < 3 else 2 * J - 3
 
-    def par(x):
-        return (x >> 1) & 1
+    def bpar(J):
+        return (J >> 1) & 1
 
     def producer():
-        order = []
-        for J in range(n_lead):
-            order.append(("K", J))
+        order = [("K", J) for J in range(min(3, N))]
         for J in range(N):
+            if J + 3 < N:
+                order.append(("K", J + 3))
             order.append(("V", J))
-            if J + 2 < N:
-                order.append(("K", J + 2))
-        q_done = set()
-        for pos, what in enumerate(order):
-            if what[0] == "K":
-                u = tiles[what[1]][0]
-                if what[1] == first[u] and u not in q_done:
-                    k = kap[u]
-                    yield lambda k=k: q_free[k % 2].ok(par(k) ^ 1)
-                    copies.append((("Q", k % 2), k))
-                    q_done.add(u)
-            assert pos == (ld_k(what[1]) if what[0] == "K" else ld_v(what[1]))
+        for pos, (kind, J) in enumerate(order):
+            assert pos == (ld_k(J) if kind == "K" else ld_v(J))
             sidx, ph = pos % nstage, (pos // nstage) & 1
             yield lambda sidx=sidx, ph=ph: kv_empty[sidx].ok(ph ^ 1)
-            copies.append((sidx, what))
-            if what[0] == "V":
-                st["v_issued"] = what[1] + 1
+            copies.append((sidx, (kind, J)))
+            if kind == "V":
+                st["v_issued"] = J + 1
 
     def pad_warp():
         for i, J in enumerate(pad_order):
@@ -750,73 +731,111 @@ def run_chain(units, nstage, seed, pad=None, chain_pv=True):
             st["cleaned"] = i + 1
 
     def mma(p):
-        seen_units = set()
-        for J in range(p, N, 2):
-            u, j = tiles[J]
-            k = kap[u]
-            if u not in seen_units:
-                yield lambda k=k: q_full[k % 2].ok(par(k))
-                seen_units.add(u)
+        if N <= p:
+            return
+        seen = [-1]
+
+        def issue_qk(J):
+            k = tiles[J][2]
+            if k != seen[0]:
+                if q_handoff == "count":
+                    yield lambda k=k: st["q_ready"] > k
+                else:
+                    yield lambda k=k: q_full.ok(k & 1)
+                seen[0] = k
             pos = ld_k(J)
             sidx, ph = pos % nstage, (pos // nstage) & 1
             yield lambda sidx=sidx, ph=ph: kv_full[sidx].ok(ph)
             if J >= 2:
-                yield lambda J=J: pv_done[p].ok(par(J - 2))
-            queues[p].extend([("qk", J, sidx, ("S", J % 2)), ("commit", s_full[J % 2]), ("commit", kv_empty[sidx])])
-            # O += P V_J
-            yield lambda J=J: p_ready[J % 2].ok(par(J))
+                yield lambda J=J: s_read[J & 1].ok(bpar(J - 2))
+            queues[p].extend([("qk", J, sidx, ("S", J & 1)), ("commit", s_full[J & 1]), ("commit", kv_empty[sidx])])
+
+        yield from issue_qk(p)
+        if p == 1 and N > 2:
+            yield from issue_qk(2)
+        for J in range(p, N, 2):
+            u, j, k = tiles[J]
             pos = ld_v(J)
             sidx, ph = pos % nstage, (pos // nstage) & 1
             yield lambda sidx=sidx, ph=ph: kv_full[sidx].ok(ph)
-            if chain_pv and J >= 1:
-                yield lambda J=J: pv_done[1 - p].ok(par(J - 1))
-            if j == 0:
-                yield lambda k=k: o_free[k % 2].ok(par(k) ^ 1)
+            yield lambda J=J: p_ready[J & 1].ok(bpar(J))
+            if j == 0 and k >= 1 and o_free_wait:
+                yield lambda k=k: o_free.ok((k - 1) & 1)
             if J in pad:
                 idx = pad_order.index(J)
                 yield lambda idx=idx: st["cleaned"] > idx
-            queues[p].extend([("pv", J, sidx, ("O", k % 2)), ("commit", pv_done[p]), ("commit", kv_empty[sidx])])
-            if J == last[u]:
-                queues[p].append(("commit", o_full[k % 2]))
+            queues[p].extend([("pv", J, sidx, ("O",)), ("commit", pv_done[p]), ("commit", kv_empty[sidx])])
+            if j == units[u] - 1:
+                queues[p].append(("commit", o_full))
+            if J + 3 < N:
+                yield from issue_qk(J + 3)
 
     def softmax():
+        J = 0
         for u, n in enumerate(units):
             if not n:
                 continue
             k = kap[u]
             for j in range(n):
-                J = first[u] + j
-                yield lambda J=J: s_full[J % 2].ok(par(J))
-                if st["S"][J % 2] != J:
-                    errors.append(f"softmax reads S_{J % 2} holding {st['S'][J % 2]} for tile {J}")
+                yield lambda J=J: s_full[J & 1].ok(bpar(J))
+                if st["S"][J & 1] != J:
+                    errors.append(f"softmax reads S_{J & 1} holding {st['S'][J & 1]} for tile {J}")
                 if j == n - 1:
-                    q_free[k % 2].arrive()   # every Q K^T of the unit has completed
-                if j > 0 and rng.random() < 0.4:   # the running max grew: rescale O
-                    yield lambda J=J: pv_done[(J - 1) % 2].ok(par(J - 1))
-                    if st["O"][k % 2] != (u, j):
-                        errors.append(f"softmax rescales O_{k % 2} holding {st['O'][k % 2]} at tile {j} of unit {u}")
-                st["P"][J % 2] = J
-                st["S"][J % 2] = None
-                p_ready[J % 2].arrive()
-            yield lambda k=k: o_free[k % 2].ok(par(k) ^ 1)
-            st["l"][k % 2] = u
-            l_full[k % 2].arrive()
+                    q_free.arrive()  # every Q K^T of the unit has completed
+                if j > 0 and rng.random() < 0.4:  # the running max grew: rescale O
+                    yield lambda J=J: pv_done[(J - 1) & 1].ok(bpar(J - 1))
+                    if st["O"] != (u, j):
+                        errors.append(f"softmax rescales O holding {st['O']} at tile {j} of unit {u}")
+                st["S"][J & 1] = ("read", J)
+                s_read[J & 1].arrive()
+                if J > 0:
+                    yield lambda J=J: pv_done[(J - 1) & 1].ok(bpar(J - 1))
+                st["P"] = J
+                p_ready[J & 1].arrive()
+                J += 1
+            yield lambda k=k: l_free[k & 1].ok(((k >> 1) & 1) ^ 1)
+            st["l"][k & 1] = u
+            l_full[k & 1].arrive()
 
-    def epilogue():
+    def unit_warps():
+        prev = None
+
+        def epilogue(u, k, n):
+            yield lambda k=k: o_full.ok(k & 1)
+            yield lambda k=k: l_full[k & 1].ok((k >> 1) & 1)
+            if st["O"] != (u, n):
+                errors.append(f"epilogue of unit {u} reads O holding {st['O']}")
+            if st["l"][k & 1] != u:
+                errors.append(f"epilogue of unit {u} reads the row sums of unit {st['l'][k & 1]}")
+            st["O_read"] = True
+            l_free[k & 1].arrive()
+            o_free.arrive()
+
+        if N:
+            copies.append(("Qs", 0))
         for u, n in enumerate(units):
             if not n:
                 continue
             k = kap[u]
-            yield lambda k=k: o_full[k % 2].ok(par(k))
-            yield lambda k=k: l_full[k % 2].ok(par(k))
-            if st["O"][k % 2] != (u, n):
-                errors.append(f"epilogue of unit {u} reads O_{k % 2} holding {st['O'][k % 2]}")
-            if st["l"][k % 2] != u:
-                errors.append(f"epilogue of unit {u} reads the l of unit {st['l'][k % 2]}")
-            st["O_read"][k % 2] = True
-            o_free[k % 2].arrive()
-
-    pending_pv = {}
+            if k >= 1 and q_free_wait:
+                yield lambda k=k: q_free.ok((k - 1) & 1)
+            yield lambda k=k: q_sfull.ok(k & 1)
+            if st["Qs"] != k:
+                errors.append(f"unit warps copy the shared Q buffer holding {st['Qs']} as Q of unit {k}")
+            for p in (0, 1):
+                for op in queues[p]:
+                    if op[0] == "qk" and tiles[op[1]][2] != k:
+                        errors.append(f"Q of unit {k} overwrites tensor memory before Q K^T of tile {op[1]}")
+            st["Qt"] = k
+            if k + 1 < kappa:  # the shared buffer is read out: load the next unit's Q into it
+                copies.append(("Qs", k + 1))
+            st["q_ready"] += 1
+            q_full.arrive()
+            if prev is not None:
+                yield from epilogue(*prev)
+            prev = (u, k, n)
+        if prev is not None:
+            yield from epilogue(*prev)
 
     def execute(p):
         op = take_tensor_op(queues[p], rng)
@@ -824,36 +843,33 @@ def run_chain(units, nstage, seed, pad=None, chain_pv=True):
             op[1].arrive()
             return
         kind, J, sidx, acc = op
-        u, j = tiles[J]
-        k = kap[u]
+        u, j, k = tiles[J]
         if kind == "qk":
             if st["stage"][sidx] != ("K", J):
                 errors.append(f"Q K^T of tile {J} reads stage {sidx} holding {st['stage'][sidx]}")
-            if st["Q"][k % 2] != k:
-                errors.append(f"Q K^T of tile {J} (kappa {k}) reads Q buffer {k % 2} holding {st['Q'][k % 2]}")
-            if st["P"][J % 2] is not None and J - 2 >= 0 and (J - 2) not in pending_pv.get("done", set()):
-                errors.append(f"Q K^T of tile {J} overwrites P of tile {st['P'][J % 2]} before its P V")
-            st["S"][J % 2] = J
-            st["P"][J % 2] = None
+            if st["Qt"] != k:
+                errors.append(f"Q K^T of tile {J} (unit {k}) reads the Q of unit {st['Qt']}")
+            if isinstance(st["S"][J & 1], int):
+                errors.append(f"Q K^T of tile {J} overwrites unread scores of tile {st['S'][J & 1]}")
+            st["S"][J & 1] = J
         else:
             if st["stage"][sidx] != ("V", J):
                 errors.append(f"P V of tile {J} reads stage {sidx} holding {st['stage'][sidx]}")
-            if st["P"][J % 2] != J:
-                errors.append(f"P V of tile {J} reads P of tile {st['P'][J % 2]}")
+            if st["P"] != J:
+                errors.append(f"P V of tile {J} reads P of tile {st['P']}")
             if J in pad and J not in st["zeroed"]:
                 errors.append(f"P V of tile {J} reads V before its padding rows were zeroed")
             if j == 0:
-                if not st["O_read"][k % 2]:
-                    errors.append(f"P V of tile {J} overwrites O_{k % 2} before the epilogue read it")
-                st["O"][k % 2], st["O_read"][k % 2] = (u, 1), False
+                if not st["O_read"]:
+                    errors.append(f"P V of tile {J} overwrites O before the epilogue read it")
+                st["O"], st["O_read"] = (u, 1), False
             else:
-                if st["O"][k % 2] != (u, j):
-                    errors.append(f"P V of tile {J} accumulates onto O_{k % 2} holding {st['O'][k % 2]}")
-                st["O"][k % 2] = (u, j + 1)
-            pending_pv.setdefault("done", set()).add(J)
+                if st["O"] != (u, j):
+                    errors.append(f"P V of tile {J} accumulates onto O holding {st['O']}")
+                st["O"] = (u, j + 1)
 
     roles = {"producer": producer(), "mma0": mma(0), "mma1": mma(1), "softmax": softmax(),
-             "epilogue": epilogue()}
+             "units": unit_warps()}
     if pad:
         roles["pad"] = pad_warp()
     waits = {}
@@ -862,18 +878,7 @@ def run_chain(units, nstage, seed, pad=None, chain_pv=True):
             waits[name] = next(roles[name])
         except StopIteration:
             del roles[name]
-    # two P V products of one O may not be in flight at once (one accumulator,
-    # two issuing threads): checked whenever a P V is issued
     while roles or queues[0] or queues[1] or copies:
-        for p in (0, 1):
-            mine = [op for op in queues[p] if op[0] == "pv"]
-            other = [op for op in queues[1 - p] if op[0] == "pv"]
-            for a in mine:
-                for b in other:
-                    if a[3] == b[3]:
-                        errors.append(f"P V of tiles {a[1]} and {b[1]} in flight together on {a[3]}")
-        if errors:
-            return errors
         moves = [("role", r) for r in roles if waits[r]()]
         moves += [("tensor", p) for p in (0, 1) if queues[p]]
         moves += [("copy", i) for i in range(len(copies))]
@@ -889,9 +894,9 @@ def run_chain(units, nstage, seed, pad=None, chain_pv=True):
             execute(x)
         else:
             dst, what = copies.pop(x)
-            if isinstance(dst, tuple):
-                st["Q"][dst[1]] = what
-                q_full[dst[1]].arrive()
+            if dst == "Qs":
+                st["Qs"] = what
+                q_sfull.arrive()
             else:
                 st["stage"][dst] = what
                 kv_full[dst].arrive()
@@ -904,7 +909,7 @@ def _chain_units(rng):
     return [rng.choice([0, 1, 1, 2, 3, 4, 4, 6]) for _ in range(rng.randint(1, 8))]
 
 
-@pytest.mark.parametrize("nstage", [3, 4, 5, 7])
+@pytest.mark.parametrize("nstage", [4, 6, 7])
 def test_chain_pipeline_is_clean(nstage):
     rng = random.Random(100 + nstage)
     for trial in range(400):
@@ -918,19 +923,22 @@ def test_chain_padding_tiles():
         units = _chain_units(rng)
         n = sum(units)
         pad = sorted(rng.sample(range(n), min(n, 3))) if n else []
-        assert run_chain(units, 5, trial, pad=pad) == [], f"units {units}, pad {pad}, seed {trial}"
+        assert run_chain(units, 6, trial, pad=pad) == [], f"units {units}, pad {pad}, seed {trial}"
 
 
-def test_chain_without_the_cross_thread_pv_wait_overlaps_products():
-    bad = sum(bool(run_chain([4, 3, 4], 5, trial, chain_pv=False)) for trial in range(300))
+def test_chain_parity_handoff_of_q_can_alias():
+    # an MMA thread may issue no score product of a one-tile unit, and then a
+    # phase wait no longer tells unit k's Q from unit k - 2's
+    rng = random.Random(11)
+    bad = sum(bool(run_chain(_chain_units(rng), 6, trial, q_handoff="parity")) for trial in range(1500))
     assert bad > 0
 
 
-def test_chain_two_stage_ring_aliases():
-    # two MMA threads consume the ring in interleaved order: with two stages
-    # one thread can wait on a stage whose previous fill, meant for the other
-    # thread, has not landed yet, and pass its parity wait on the fill before
-    # that; the kernel keeps at least three stages
-    rng = random.Random(102)
-    bad = sum(bool(run_chain(_chain_units(rng), 2, trial)) for trial in range(200))
+def test_chain_without_the_o_free_wait_overwrites_o():
+    bad = sum(bool(run_chain([3, 2, 4, 1, 3], 6, trial, o_free_wait=False)) for trial in range(300))
+    assert bad > 0
+
+
+def test_chain_without_the_q_free_wait_overwrites_q():
+    bad = sum(bool(run_chain([3, 2, 4, 1, 3], 6, trial, q_free_wait=False)) for trial in range(300))
     assert bad > 0

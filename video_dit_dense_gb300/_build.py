@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libh3attn.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["api.cu", "qk_norm_rope.cu", "attn_fwd.cu", "rmsnorm_modulate.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "attn_pipe.cuh", "attn_persist.cuh", "attn_wide.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "attn_pipe.cuh", "attn_persist.cuh", "attn_wide.cuh", "attn_chain.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                      "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

@@ -187,7 +187,7 @@ namespace {
 // Kernel choice override (tests run every case on every kernel): "1" .. "5".
 int kernel_override() {
   const char* kern = getenv("H3ATTN_ATTN_KERNEL");
-  return (kern && kern[0] >= '1' && kern[0] <= '5') ? kern[0] - '0' : 0;
+  return (kern && kern[0] >= '1' && kern[0] <= '6') ? kern[0] - '0' : 0;
 }
 
 // The fields of AttnArgs that decide the kernel and the split-key plan.

@@ -156,6 +156,20 @@ __device__ __forceinline__ bool count_wait_sleep(uint32_t addr, uint32_t target,
   }
   return true;
 }
+// mbar_wait for the same kind of warp.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_test_wait(bar, parity)) {
+    if (*ctl.abort_flag) return false;
+    if (globaltimer_ns() - t0 > ctl.limit_ns) {
+      *ctl.abort_flag = 1u;
+      atomicExch(ctl.status, ctl.timeout_code);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
 
 // Keys past kv_len may hold anything (uninitialised padding, NaN, Inf).  Their
 // scores are masked by selection, but in O += P V a zero probability times a
@@ -559,6 +573,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
 #include "attn_pipe.cuh"
 #include "attn_persist.cuh"
 #include "attn_wide.cuh"
+#include "attn_chain.cuh"
 
 template <int D, int NQ, int NSTAGE, int CTAS = 1>
 cudaError_t launch_cfg(const AttnArgs& a, cudaStream_t stream) {
@@ -655,7 +670,10 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   //      (P over its score buffer, Q and half-tiles of K/V in shared memory);
   //   2  two query tiles per CTA sharing each K/V tile (head_dim 256: one
   //      tile with a single score buffer), only on request;
-  //   3  the persistent kernel (one CTA per SM over all units), on request.
+  //   3  the persistent kernel (one CTA per SM over all units), on request;
+  //   6  head_dim 128: one CTA per SM chaining its work units (a unit's Q
+  //      load, scores and softmax overlap the previous unit's last products
+  //      and epilogue), on request.
   // a.kernel: 0 = by shape, else the kernel above (head dims it lacks fall
   // back to the shape rule's next choice).
   if (a.split_pieces > 0) {  // planned by plan_split: the one-query-tile kernel
@@ -663,7 +681,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     if (a.D == 128) return launch_pipe<128, 7>(a, stream);
     return cudaErrorInvalidValue;
   }
-  if (a.kernel == 5 && a.D != 256) {  // head dims without a wide kernel: the shape rule below
+  if (a.kernel == 6 && a.D == 128 && a.win_ct == 0) return launch_chain<5>(a, stream);
+  if ((a.kernel == 5 && a.D != 256) || a.kernel == 6) {  // head dims without that kernel: the shape rule below
     AttnArgs b = a;
     b.kernel = 0;
     return launch_attention(b, stream);

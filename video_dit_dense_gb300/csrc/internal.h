@@ -88,7 +88,8 @@ struct AttnArgs {
   uint64_t wait_limit_ns;
   int debug_skip_producer;  // fault injection for the bounded-wait test: 1 = never load K/V
   // 0 = choose by head dim and key length; 1 = one query tile per CTA (Q in tensor memory),
-  // 2 = two query tiles per CTA, 3 = persistent (one CTA per SM), 4 = one query tile, two CTAs per SM
+  // 2 = two query tiles per CTA, 3 = persistent (one CTA per SM), 4 = one query tile, two CTAs per SM,
+  // 5 = head dim 256 with double-buffered scores, 6 = head dim 128, one CTA per SM chaining its units
   int kernel;
   // chunked window (self-attention, one-query-tile kernel only): tokens per
   // chunk (0 = dense), anchor tokens, radius in chunks
