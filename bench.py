@@ -499,9 +499,10 @@ def _time_window(h3, gen, torch, stream, peaks, steps=5, warmup=3):
 # The library's choice of attention kernel: one query tile per CTA (Q held in
 # tensor memory) for head dim 128 from 1024 keys on; one query tile per CTA
 # with two CTAs per SM for head dim 128 below that and for head dim 64; the
-# two-tile kernel's code with one tile for head dim 256.  H3ATTN_ATTN_KERNEL
-# forces 1 (one tile, Q in tensor memory), 2 (two tiles per CTA), 3 (the
-# persistent kernel) or 4 (two CTAs per SM) where the head dim has it.
+# double-buffered-score kernel for head dim 256.  H3ATTN_ATTN_KERNEL forces 1
+# (one tile, Q in tensor memory), 2 (two tiles per CTA), 3 (the persistent
+# kernel), 4 (two CTAs per SM), 5 (head dim 256) or 6 (the unit-chaining
+# kernel, head dim 128) where the head dim has it.
 ONE_TILE_MIN_KEYS = 1024
 
 
@@ -509,6 +510,8 @@ def _attn_kernel_name(wl):
     sel = os.environ.get("H3ATTN_ATTN_KERNEL", "")
     if wl.D == 256:
         return "attn_fwd_kernel<256,1,2,1>" if sel in ("2", "3", "4") else "attn_wide_kernel<5>"
+    if sel == "6" and wl.D == 128:
+        return "attn_chain_kernel<6>"
     if sel == "3":
         return {64: "attn_persist_kernel<64,12>", 128: "attn_persist_kernel<128,7>"}[wl.D]
     one_tile = sel == "1" or (sel not in ("2", "4") and wl.D == 128 and wl.Sk >= ONE_TILE_MIN_KEYS)

@@ -266,7 +266,7 @@ h3attn_status_t prefill(const void* q, const void* k, const void* v, void* o, in
     }
   }
   if (!make_bshd_map(&a.tm_q, q, B, Sq, Hq, D) || !make_bshd_map(&a.tm_k, k, B, Sk, Hkv, D) ||
-      !make_bshd_map(&a.tm_v, v, B, Sk, Hkv, D))
+      !make_bshd_map(&a.tm_v, v, B, Sk, Hkv, D) || !make_bshd_map(&a.tm_o, o, B, Sq, Hq, D))
     return H3ATTN_ERR_LAUNCH;
   a.q_ptr = static_cast<const uint16_t*>(q);
   a.o = static_cast<uint16_t*>(o);

@@ -38,8 +38,8 @@ struct PipeCfg {
   static constexpr int kChunkBytes = kBlockM * 128;
   static constexpr int kSmemKV = NSTAGE * kTileBytes;
   // q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_read[2], p_ready[2], pv_done[2], drain[2],
-  // v_clean
-  static constexpr int kNumBars = 1 + 2 * NSTAGE + 11;
+  // v_clean, o_staged
+  static constexpr int kNumBars = 1 + 2 * NSTAGE + 12;
   static constexpr int kSmemBytes = 1024 + kSmemKV + kNumBars * 8 + 16;
   static constexpr int kThreads = 256;
   static constexpr int kProducerWarp = 4;
@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
   auto bar_pv_done = [&](int p) { return bars + 8u * (7 + 2 * NSTAGE + p); };
   auto bar_drain = [&](int p) { return bars + 8u * (9 + 2 * NSTAGE + p); };
   const uint32_t bar_v_clean = bars + 8u * (11 + 2 * NSTAGE);
+  const uint32_t bar_o_staged = bars + 8u * (12 + 2 * NSTAGE);  // o rows staged for the TMA store (128 softmax)
   uint8_t* gmisc = gbase + C::kSmemKV + C::kNumBars * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gmisc + 4);
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       mbar_init(bar_drain(p), 1);
     }
     mbar_init(bar_v_clean, 1);
+    mbar_init(bar_o_staged, 128);
     *abort_flag = 0u;
     *reinterpret_cast<volatile uint32_t*>(gmisc + 8) = 0u;  // pad_issued
     fence_barrier_init();
@@ -540,28 +542,46 @@ __global__ void __launch_bounds__(256, 1) attn_pipe_kernel(const __grid_constant
       part[kBlockM * D + t] = m_ref;
       part[kBlockM * D + kBlockM + t] = l;
     } else if (ok) {
-      const bool live_row = row < a.Sq;
+      // o = O / l as bf16, staged in the K/V ring (idle now: every load has
+      // landed and been consumed once the last P V is complete) in the
+      // 128-byte swizzled layout of the o map's box, then one TMA store of
+      // the tile; rows past Sq lie outside the tensor and are not written.
+      // (One row per thread straight to global memory writes 32 rows apart
+      // per warp instruction; the CTA's end took ~4.8 k cycles that way.)
       const bool zero_row = row >= q_lim || n_tiles == 0 || !(l > 0.0f);
       const float inv = zero_row ? 0.0f : 1.0f / l;
-      uint16_t* orow = a.o + ((static_cast<int64_t>(b) * a.Sq + row) * a.Hq + h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         if (n_tiles > 0) {
           tmem_ld32(tO + c * 32, o);
           tmem_ld_wait(o);
-        }
-        if (live_row) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        } else {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = zero_row ? 0.0f : __uint_as_float(o[v * 8 + e]) * inv;
-            dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                                pack_bf16x2(f[6], f[7]));
-          }
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
+        // channels [32c, 32c + 32): 16-byte units 4(c mod 2) .. +3 of row t in swizzle column c / 2
+        const uint32_t rowp = sKV + (c >> 1) * C::kChunkBytes + t * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = zero_row ? 0u
+                            : pack_bf16x2(__uint_as_float(o[v * 8 + 2 * e]) * inv,
+                                          __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           rowp + ((((c & 1) * 4 + v) ^ (t & 7)) << 4)),
+                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar_o_staged);
+      if (t == 0 && mbar_wait(bar_o_staged, 0, ctl)) {
+        for (int c = 0; c < C::kChunks; ++c) tma_store_4d(&a.tm_o, sKV + c * C::kChunkBytes, c * 64, h, q0, b);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the shared-memory source is read before the CTA retires
       }
     }
   }

@@ -37,8 +37,8 @@ struct WideCfg {
   static constexpr int kChunk = kBlockN * 128;          // 16 KiB: one 64-channel swizzle column
   static constexpr int kQBytes = kBlockM * D * 2;       // 64 KiB
   static constexpr int kSmemKV = NSTAGE * kHalfBytes;
-  // q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_ready[2], pv_done, drain, v_clean
-  static constexpr int kNumBars = 1 + 2 * NSTAGE + 2 + 2 + 3;
+  // q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], p_ready[2], pv_done, drain, v_clean, o_staged
+  static constexpr int kNumBars = 1 + 2 * NSTAGE + 2 + 2 + 4;
   static constexpr int kSmemBytes = 1024 + kQBytes + kSmemKV + kNumBars * 8 + 16;
   static constexpr int kThreads = 256;
   static constexpr int kProducerWarp = 4;
@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
   const uint32_t bar_pv_done = bars + 8u * (5 + 2 * NSTAGE);
   const uint32_t bar_drain = bars + 8u * (6 + 2 * NSTAGE);
   const uint32_t bar_v_clean = bars + 8u * (7 + 2 * NSTAGE);
+  const uint32_t bar_o_staged = bars + 8u * (8 + 2 * NSTAGE);  // o rows staged for the TMA store (128 softmax)
   uint8_t* gmisc = gbase + C::kQBytes + C::kSmemKV + C::kNumBars * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gmisc + 4);
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
     mbar_init(bar_pv_done, 1);
     mbar_init(bar_drain, 1);
     mbar_init(bar_v_clean, 1);
+    mbar_init(bar_o_staged, 128);
     *abort_flag = 0u;
     *reinterpret_cast<volatile uint32_t*>(gmisc + 8) = 0u;  // pad_issued
     fence_barrier_init();
@@ -371,28 +373,43 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
       tc_fence_after();
     }
     if (ok) {
-      const bool live_row = row < a.Sq;
+      // o = O / l as bf16, staged over Q in shared memory (every product has
+      // completed) in the 128-byte swizzled layout of the o map's box, then
+      // one TMA store of the tile; rows past Sq are not written.
       const bool zero_row = row >= q_lim || n_tiles == 0 || !(l > 0.0f);
       const float inv = zero_row ? 0.0f : 1.0f / l;
-      uint16_t* orow = a.o + ((static_cast<int64_t>(b) * a.Sq + row) * a.Hq + h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         if (n_tiles > 0) {
           tmem_ld32(tO + c * 32, o);
           tmem_ld_wait(o);
-        }
-        if (live_row) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        } else {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = zero_row ? 0.0f : __uint_as_float(o[v * 8 + e]) * inv;
-            dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                                pack_bf16x2(f[6], f[7]));
-          }
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
+        // channels [32c, 32c + 32): 16-byte units 4(c mod 2) .. +3 of row t in swizzle column c / 2
+        const uint32_t rowp = sQ + (c >> 1) * C::kChunk + t * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = zero_row ? 0u
+                            : pack_bf16x2(__uint_as_float(o[v * 8 + 2 * e]) * inv,
+                                          __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           rowp + ((((c & 1) * 4 + v) ^ (t & 7)) << 4)),
+                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar_o_staged);
+      if (t == 0 && mbar_wait(bar_o_staged, 0, ctl)) {
+        for (int c = 0; c < D / 64; ++c) tma_store_4d(&a.tm_o, sQ + c * C::kChunk, c * 64, h, q0, b);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the shared-memory source is read before the CTA retires
       }
     }
   }

@@ -76,6 +76,7 @@ cudaError_t launch_rmsnorm_modulate(const ModArgs& a, cudaStream_t stream);
 // ---- dense prefill attention ----
 struct AttnArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D (D, H, S, B) bf16 maps, 64-element inner box, 128B swizzle
+  CUtensorMap tm_o;              // the same over o (epilogues that store a staged tile with TMA)
   const uint16_t* q_ptr;         // q itself (kernels that stage Q through registers)
   uint16_t* o;
   const int32_t* kv_len;
