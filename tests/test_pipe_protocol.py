@@ -660,8 +660,9 @@ def run_chain(units, nstage, seed, pad=None, q_handoff="count", o_free_wait=True
     previous P V has completed.  At unit changes:
       Q: the unit warps copy Q_kappa from a single shared-memory buffer
         into the single tensor-memory Q buffer once the softmax has seen the
-        last score tile of unit kappa - 1 (its Q K^T are then complete), then
-        load Q_{kappa+1} into the shared buffer themselves (the producer,
+        last score tile of unit kappa - 1 (its Q K^T are then complete), send
+        o of unit kappa - 1 out through the shared buffer, then load
+        Q_{kappa+1} into it themselves (the producer,
         which runs three tiles ahead over several short units, would have to
         wait for that copy before its next K load: a cycle through the
         epilogue, which waits for a P V whose V comes after that K), and
@@ -827,12 +828,12 @@ def run_chain(units, nstage, seed, pad=None, q_handoff="count", o_free_wait=True
                     if op[0] == "qk" and tiles[op[1]][2] != k:
                         errors.append(f"Q of unit {k} overwrites tensor memory before Q K^T of tile {op[1]}")
             st["Qt"] = k
-            if k + 1 < kappa:  # the shared buffer is read out: load the next unit's Q into it
-                copies.append(("Qs", k + 1))
             st["q_ready"] += 1
             q_full.arrive()
             if prev is not None:
-                yield from epilogue(*prev)
+                yield from epilogue(*prev)  # o of the previous unit goes out through the buffer
+            if k + 1 < kappa:  # then the next unit's Q comes in through it
+                copies.append(("Qs", k + 1))
             prev = (u, k, n)
         if prev is not None:
             yield from epilogue(*prev)

@@ -22,16 +22,17 @@
 //   O         [320, 448)           output accumulator of the current unit (fp32)
 //   Q         [448, 512)           query rows of the current unit (bf16 pairs),
 //                                  the A operand of S = Q K^T
-// Shared memory: one Q staging buffer (32 KiB, TMA, 128-byte swizzle), a ring
-// of NSTAGE K/V tiles (32 KiB each), barriers, the row sums handed from the
-// softmax to the epilogue (two slots).
+// Shared memory: one 32 KiB buffer through which Q tiles come in and o tiles
+// go out (TMA, 128-byte swizzle), a ring of NSTAGE K/V tiles (32 KiB each),
+// barriers, the row sums handed from the softmax to the epilogue (two slots).
 //
 // Unit changes (kappa = rank of a unit among the CTA's units with key tiles;
 // units without any, rows past q_len or kv_len 0, only get zero rows):
-//   Q: the unit warps copy Q_kappa from the staging buffer into tensor memory
-//      once the softmax has seen the last score tile of unit kappa - 1 (every
+//   Q: the unit warps copy Q_kappa from the buffer into tensor memory once
+//      the softmax has seen the last score tile of unit kappa - 1 (every
 //      Q K^T of that unit has then completed), count the copy into q_ready,
-//      and load Q_{kappa+1} into the staging buffer themselves.  An MMA thread
+//      and load Q_{kappa+1} into the buffer themselves once o of unit
+//      kappa - 1 has gone out through it.  An MMA thread
 //      waits for q_ready >= 128 (kappa + 1) before its first Q K^T of unit
 //      kappa: a count, because a thread may issue no score product of a
 //      one-tile unit, after which a phase bit no longer tells unit kappa's Q
@@ -40,8 +41,9 @@
 //      several short units: the copy waits for the epilogue of an earlier
 //      unit, whose P V needs a V load queued behind that K.)
 //   O: the MMA thread of a unit's last tile commits o_full after its P V; the
-//      unit warps read O and the row sums, write o = O / l as bf16 and free O;
-//      the next unit's first P V (no accumulate) waits for that.
+//      unit warps read O and the row sums and free O (the next unit's first
+//      P V, no accumulate, waits for that), stage o = O / l as bf16 in the
+//      buffer and write it with one TMA store.
 // Every hand-off is a barrier that completes once per use (or a count), and
 // each waiter can show that at most the awaited phase is pending; the CPU
 // model of this protocol in the tests runs random interleavings of it.
@@ -60,7 +62,7 @@ struct ChainCfg {
   static constexpr int kQBytes = kBlockM * D * 2;
   static constexpr int kSmemKV = NSTAGE * kTileBytes;
   // kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_read[2], p_ready[2], pv_done[2], drain[2],
-  // q_sfull, q_sfree, q_free, o_full, o_free, l_full[2], l_free[2]
+  // q_sfull, buf_free, q_free, o_full, o_free, l_full[2], l_free[2]
   static constexpr int kNumBars = 2 * NSTAGE + 10 + 5 + 4;
   static constexpr int kMiscBytes = 32 + 2 * kBlockM * 4;  // slot, abort, counts; row sums [2][128]
   static constexpr int kSmemBytes = 1024 + kQBytes + kSmemKV + kNumBars * 8 + kMiscBytes;
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(384, 1) attn_chain_kernel(const __grid_constan
   auto bar_drain = [&](int p) { return bars + 8u * (2 * NSTAGE + 8 + p); };
   // once per unit with key tiles
   const uint32_t bar_q_sfull = bars + 8u * (2 * NSTAGE + 10);  // Q_kappa in the staging buffer
-  const uint32_t bar_q_sfree = bars + 8u * (2 * NSTAGE + 11);  // staging buffer read out (128 unit threads)
+  const uint32_t bar_buf_free = bars + 8u * (2 * NSTAGE + 11);  // the unit threads are done with the buffer
   const uint32_t bar_q_free = bars + 8u * (2 * NSTAGE + 12);   // every Q K^T of the unit done (128 softmax)
   const uint32_t bar_o_full = bars + 8u * (2 * NSTAGE + 13);   // the unit's last P V done
   const uint32_t bar_o_free = bars + 8u * (2 * NSTAGE + 14);   // O read out (128 unit threads)
@@ -235,7 +237,7 @@ __global__ void __launch_bounds__(384, 1) attn_chain_kernel(const __grid_constan
       mbar_init(bar_l_free(p), 128);
     }
     mbar_init(bar_q_sfull, 1);
-    mbar_init(bar_q_sfree, 128);
+    mbar_init(bar_buf_free, 128);
     mbar_init(bar_q_free, 128);
     mbar_init(bar_o_full, 1);
     mbar_init(bar_o_free, 128);
@@ -533,15 +535,24 @@ __global__ void __launch_bounds__(384, 1) attn_chain_kernel(const __grid_constan
   } else {
     regs_dec<C::kUnitRegs>();
     // ======================= unit warps: Q hand-off, epilogue ==============
-    // (their waits sleep between polls: these warps share SM sub-partitions
-    // with the softmax warps, whose issue slots set the pace)
+    // One shared-memory buffer serves both hand-offs.  Per unit with key
+    // tiles: Q_kap is copied out of it into tensor memory; o of the previous
+    // unit is staged into it (128-byte swizzled rows, the o map's box) once
+    // that unit's O and row sums are complete; then, once every unit thread is
+    // done with the buffer, one thread writes that o with one TMA store and,
+    // when the store has read the buffer, loads Q_{kap+1} into it.  (One row
+    // per thread stored straight to global memory took 3.5-4.2 k cycles per
+    // unit and held back the next unit's first P V.)  The waits park the
+    // warps in the barrier wait: they share SM sub-partitions with the
+    // softmax warps, whose issue slots set the pace.
     const int wq = warp & 3;
     const int t = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tO = tmem + lane_off + C::kColO;
     bool ok = true;
-    int kap = -1, q_loaded = -1, q_taken = -1;  // units whose Q was loaded / copied out (thread 0)
-    auto load_q = [&](int u) {  // Q of unit u (with key tiles) into the staging buffer
+    // thread 0: phases of buf_free waited, units whose Q was loaded / copied out
+    int kap = -1, uses = 0, q_loaded = -1, q_taken = -1;
+    auto load_q = [&](int u) {  // Q of unit u (with key tiles) into the buffer
       const ChainUnit c = chain_unit(a, u, nqb);
       mbar_arrive_expect_tx(bar_q_sfull, C::kQBytes);
       for (int ch = 0; ch < 2; ++ch)
@@ -553,19 +564,17 @@ __global__ void __launch_bounds__(384, 1) attn_chain_kernel(const __grid_constan
         if (chain_unit(a, u, nqb).n > 0) return u;
       return n_units;
     };
-    // o = O / l as bf16 for the unit of rank pk (slot pk mod 2)
-    auto epilogue = [&](const ChainUnit& c, int pk) -> bool {
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar_o_full, pk & 1, ctl) &&
-                                       mbar_wait_sleep(bar_l_full(pk & 1), bpar(pk), ctl)))
+    // o = O / l as bf16 rows of the unit of rank pk (row-sum slot pk mod 2) into the buffer
+    auto stage_o = [&](const ChainUnit& c, int pk) -> bool {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_parked(bar_o_full, pk & 1, ctl) &&
+                                       mbar_wait_parked(bar_l_full(pk & 1), bpar(pk), ctl)))
         return false;
       if (t == 0) H3_TRACE(kEvSmLd1, pk);
       tc_fence_after();
       const float l = lbuf[(pk & 1) * kBlockM + t];
       mbar_arrive(bar_l_free(pk & 1));
-      const int row = c.q0 + t;
-      const bool zero_row = row >= c.q_lim || !(l > 0.0f);
+      const bool zero_row = c.q0 + t >= c.q_lim || !(l > 0.0f);
       const float inv = zero_row ? 0.0f : 1.0f / l;
-      uint16_t* orow = a.o + ((static_cast<int64_t>(c.b) * a.Sq + row) * a.Hq + c.h) * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -576,19 +585,45 @@ __global__ void __launch_bounds__(384, 1) attn_chain_kernel(const __grid_constan
           mbar_arrive(bar_o_free);  // O read out: the next unit's first P V may overwrite it
           if (t == 0) H3_TRACE(kEvCtaEnd, pk);
         }
-        if (row < a.Sq) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+        // channels [32cc, 32cc + 32): 16-byte units 4(cc mod 2) .. +3 of row t in swizzle column cc / 2
+        const uint32_t rowp = sQ + (cc >> 1) * C::kChunk + t * 128;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = zero_row ? 0.0f : __uint_as_float(o[v * 8 + e]) * inv;
-            dst[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                                pack_bf16x2(f[6], f[7]));
-          }
+          for (int e = 0; e < 4; ++e)
+            w[e] = zero_row ? 0u
+                            : pack_bf16x2(__uint_as_float(o[v * 8 + 2 * e]) * inv,
+                                          __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           rowp + ((((cc & 1) * 4 + v) ^ (t & 7)) << 4)),
+                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
         }
       }
+      fence_proxy_async_smem();
       return true;
+    };
+    // Every unit thread is done with the buffer: thread 0 stores the staged o
+    // of unit pc (if has_o), then loads the Q of the next unit with key tiles
+    // after unit u (if any).
+    auto flush = [&](bool has_o, const ChainUnit& pc, int u) -> bool {
+      mbar_arrive(bar_buf_free);
+      bool r = true;
+      if (t == 0) {
+        r = mbar_wait_parked(bar_buf_free, uses & 1, ctl);
+        ++uses;
+        if (r && has_o) {
+          for (int ch = 0; ch < 2; ++ch) tma_store_4d(&a.tm_o, sQ + ch * C::kChunk, ch * 64, pc.h, pc.q0, pc.b);
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the buffer is read out before the next Q lands in it
+        }
+        if (r && u < n_units) {
+          const int nu = next_with_tiles(u);
+          if (nu < n_units) load_q(nu);
+        }
+      }
+      return __all_sync(0xFFFFFFFFu, r);
     };
     if (t == 0 && n_kap > 0) load_q(next_with_tiles(static_cast<int>(blockIdx.x) - G));
     ChainUnit prev{};
@@ -605,14 +640,14 @@ __global__ void __launch_bounds__(384, 1) attn_chain_kernel(const __grid_constan
       }
       ++kap;
       // Q_kap into tensor memory once every Q K^T of the previous unit is done
-      ok = __all_sync(0xFFFFFFFFu, (kap == 0 || mbar_wait_sleep(bar_q_free, (kap - 1) & 1, ctl)) &&
-                                       mbar_wait_sleep(bar_q_sfull, kap & 1, ctl));
+      ok = __all_sync(0xFFFFFFFFu, (kap == 0 || mbar_wait_parked(bar_q_free, (kap - 1) & 1, ctl)) &&
+                                       mbar_wait_parked(bar_q_sfull, kap & 1, ctl));
       if (!ok) break;
       if (t == 0) q_taken = kap;
       if (t == 0) H3_TRACE(kEvSmS1, kap);
       tc_fence_after();
       {
-        // row t of the staging buffer: 16-byte unit i of a 128-byte row sits at i ^ (t mod 8)
+        // row t of the buffer: 16-byte unit i of a 128-byte row sits at i ^ (t mod 8)
         const uint32_t src = sQ + t * 128;
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
@@ -628,22 +663,15 @@ __global__ void __launch_bounds__(384, 1) attn_chain_kernel(const __grid_constan
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_q_sfree);
       add_release_cta(q_ready, 1u);
       if (t == 0) H3_TRACE(kEvCtaStart, kap);
-      if (t == 0 && kap + 1 < n_kap) {
-        // the staging buffer is read out by all 128 unit threads: next unit's Q
-        ok = mbar_wait_sleep(bar_q_sfree, kap & 1, ctl);
-        if (ok) {
-          fence_proxy_async_smem();
-          load_q(next_with_tiles(u));
-        }
-      }
-      if (!(ok = __all_sync(0xFFFFFFFFu, ok))) break;  // the warp leaves together
-      if (kap >= 1 && !(ok = epilogue(prev, kap - 1))) break;
+      // o of the previous unit through the buffer (this thread's rows only: it
+      // read its own Q row above), then the next Q into it
+      if (kap >= 1 && !(ok = stage_o(prev, kap - 1))) break;
+      if (!(ok = flush(kap >= 1, prev, u))) break;
       prev = c;
     }
-    if (ok && kap >= 0) ok = epilogue(prev, kap);
+    if (ok && kap >= 0) ok = stage_o(prev, kap) && flush(true, prev, n_units);
     // Drain: a Q load issued but never waited for (the CTA aborted) lands before the CTA retires.
     if (t == 0 && q_loaded > q_taken) mbar_wait_drain(bar_q_sfull, q_loaded & 1, a.wait_limit_ns);
   }

@@ -156,17 +156,18 @@ __device__ __forceinline__ bool count_wait_sleep(uint32_t addr, uint32_t target,
   }
   return true;
 }
-// mbar_wait for the same kind of warp.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+// mbar_wait for the same kind of warp: each poll parks the thread in the
+// barrier wait (woken when the phase completes, or after the hint) instead of
+// spinning.
+__device__ __forceinline__ bool mbar_wait_parked(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_test_wait(bar, parity)) {
+  while (!mbar_try_wait_hint(bar, parity, 1000000u)) {
     if (*ctl.abort_flag) return false;
     if (globaltimer_ns() - t0 > ctl.limit_ns) {
       *ctl.abort_flag = 1u;
       atomicExch(ctl.status, ctl.timeout_code);
       return false;
     }
-    __nanosleep(64);
   }
   return true;
 }
