@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
         for (int kind = 0; kind < 2; ++kind, ++it) {
           const int s = it % NSTAGE;
           const uint32_t ph = (it / NSTAGE) & 1;
-          if (!mbar_wait(bar_kv_empty(s), ph ^ 1u, ctl)) {
+          if (!mbar_wait<kWaitParked>(bar_kv_empty(s), ph ^ 1u, ctl)) {
             ok = false;
             break;
           }
@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
     if (j_pad >= 0) {
       const int it_v = 2 * j_pad + 1;  // load index of V_{j_pad}
       const bool ok = __all_sync(0xFFFFFFFFu, count_wait_sleep(pad_issued, 1u, ctl) &&
-                                                  mbar_wait(bar_kv_full(it_v % NSTAGE), (it_v / NSTAGE) & 1, ctl));
+                                                  mbar_wait<kWaitParked>(bar_kv_full(it_v % NSTAGE), (it_v / NSTAGE) & 1, ctl));
       if (ok) {  // V tile landed; its stage is refilled only after O += P V of it
         zero_padding_rows<D>(sKV + (it_v % NSTAGE) * C::kTileBytes, kv_lim % kBlockN, lane, 32);
         __syncwarp();
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
   } else if (warp == C::kMmaWarp) {
     // ======================= MMA issuer ====================================
     if (lane == 0 && n_tiles > 0) {
-      bool ok = mbar_wait(bar_q_full, 0, ctl);
+      bool ok = mbar_wait<kWaitParked>(bar_q_full, 0, ctl);
       tc_fence_after();
       int it = 0;
       for (int j = 0; ok && j < n_tiles; ++j) {
@@ -364,12 +364,12 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
           const int s = it % NSTAGE;
           const uint32_t ph = (it / NSTAGE) & 1;
           ++it;
-          if (!(ok = mbar_wait(bar_kv_full(s), ph, ctl))) break;
+          if (!(ok = mbar_wait<kWaitParked>(bar_kv_full(s), ph, ctl))) break;
           H3_TRACE(kEvMmaK, j);
           tc_fence_after();
           for (int q = 0; q < NQ; ++q) {
             if (j > 0) {
-              if (!(ok = mbar_wait(bar_pv_done(q), (j - 1) & 1, ctl))) break;
+              if (!(ok = mbar_wait<kWaitParked>(bar_pv_done(q), (j - 1) & 1, ctl))) break;
               tc_fence_after();
             }
             H3_TRACE(kEvMmaQK0 + q, j);
@@ -391,13 +391,13 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
           const int s = it % NSTAGE;
           const uint32_t ph = (it / NSTAGE) & 1;
           ++it;
-          if (!(ok = mbar_wait(bar_kv_full(s), ph, ctl))) break;
-          if (j == j_pad && !(ok = mbar_wait(bar_v_clean, 0, ctl))) break;  // padding rows zeroed
+          if (!(ok = mbar_wait<kWaitParked>(bar_kv_full(s), ph, ctl))) break;
+          if (j == j_pad && !(ok = mbar_wait<kWaitParked>(bar_v_clean, 0, ctl))) break;  // padding rows zeroed
           H3_TRACE(kEvMmaV, j);
           tc_fence_after();
           const uint32_t vb = sKV + s * C::kTileBytes;
           for (int q = 0; q < NQ; ++q) {
-            if (!(ok = mbar_wait(bar_p_ready(q), j & 1, ctl))) break;
+            if (!(ok = mbar_wait<kWaitParked>(bar_p_ready(q), j & 1, ctl))) break;
             H3_TRACE(kEvMmaPV0 + q, j);
             tc_fence_after();
 #pragma unroll
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
     float l = 0.0f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      ok = mbar_wait(bar_s_full(q), j & 1, ctl);
+      ok = mbar_wait<kWaitParked>(bar_s_full(q), j & 1, ctl);
       if (t == 0) H3_TRACE(kEvSmS0 + 4 * q, j);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
       if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
         // O_q += P V of the previous tile has completed before this tile's
         // S_q was issued; the wait below returns at once and is kept as a guard.
-        ok = mbar_wait(bar_pv_done(q), (j - 1) & 1, ctl);
+        ok = mbar_wait<kWaitParked>(bar_pv_done(q), (j - 1) & 1, ctl);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
           ok = false;
           break;
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
     }
     // ---- epilogue: O / l -> bf16 ------------------------------------------
     if (ok && n_tiles > 0) {
-      ok = mbar_wait(bar_pv_done(q), (n_tiles - 1) & 1, ctl);
+      ok = mbar_wait<kWaitParked>(bar_pv_done(q), (n_tiles - 1) & 1, ctl);
       ok = __all_sync(0xFFFFFFFFu, ok);
       tc_fence_after();
     }
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
       }
       fence_proxy_async_smem();
       mbar_arrive(bar_o_staged(q));
-      if (t == 0 && mbar_wait(bar_o_staged(q), 0, ctl)) {
+      if (t == 0 && mbar_wait<kWaitParked>(bar_o_staged(q), 0, ctl)) {
         for (int c = 0; c < C::kChunks; ++c)
           tma_store_4d(&a.tm_o, sO + c * C::kChunkBytes, c * 64, h, q0 + q * kBlockM, b);
         bulk_commit_group();

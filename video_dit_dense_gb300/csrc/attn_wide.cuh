@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
       auto load = [&](int kind, int j) {  // both halves of K_j (kind 0) or V_j (kind 1)
         for (int half = 0; ok && half < 2; ++half) {
           const int s = stage_of(pos);
-          if (!(ok = mbar_wait(bar_kv_empty(s), phase_of(pos) ^ 1u, ctl))) return;
+          if (!(ok = mbar_wait<kWaitParked>(bar_kv_empty(s), phase_of(pos) ^ 1u, ctl))) return;
           mbar_arrive_expect_tx(bar_kv_full(s), C::kHalfBytes);
           const CUtensorMap* m = kind == 0 ? &a.tm_k : &a.tm_v;
           for (int c = 0; c < 2; ++c)
@@ -176,14 +176,14 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
   } else if (warp == C::kMmaWarp) {
     // ======================= MMA thread ====================================
     if (lane == 0 && n_tiles > 0) {
-      bool ok = mbar_wait(bar_q_full, 0, ctl);
+      bool ok = mbar_wait<kWaitParked>(bar_q_full, 0, ctl);
       tc_fence_after();
       // S_{j mod 2} = Q K_j^T: 16 MMAs of 16 channels, 8 on each half of K_j
       auto issue_qk = [&](int j) -> bool {
         const uint32_t tS = tmem + (j & 1) * 128;
         for (int half = 0; half < 2; ++half) {
           const int pos = ld_k(j) + half, s = stage_of(pos);
-          if (!mbar_wait(bar_kv_full(s), phase_of(pos), ctl)) return false;
+          if (!mbar_wait<kWaitParked>(bar_kv_full(s), phase_of(pos), ctl)) return false;
           tc_fence_after();
           const uint32_t kb = sKV + s * C::kHalfBytes;
 #pragma unroll
@@ -201,13 +201,13 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
       if (ok) ok = issue_qk(0);
       if (ok && n_tiles > 1) ok = issue_qk(1);
       for (int j = 0; ok && j < n_tiles; ++j) {
-        if (!(ok = mbar_wait(bar_p_ready(j & 1), bpar(j), ctl))) break;
-        if (j == j_pad && !(ok = mbar_wait(bar_v_clean, 0, ctl))) break;  // padding rows zeroed
+        if (!(ok = mbar_wait<kWaitParked>(bar_p_ready(j & 1), bpar(j), ctl))) break;
+        if (j == j_pad && !(ok = mbar_wait<kWaitParked>(bar_v_clean, 0, ctl))) break;  // padding rows zeroed
         // O[:, 128 half ...] += P_j V_j[:, 128 half ...]: A = P over S_{j mod 2}
         const uint32_t tP = tmem + (j & 1) * 128;
         for (int half = 0; half < 2; ++half) {
           const int pos = ld_v(j) + half, s = stage_of(pos);
-          if (!(ok = mbar_wait(bar_kv_full(s), phase_of(pos), ctl))) break;
+          if (!(ok = mbar_wait<kWaitParked>(bar_kv_full(s), phase_of(pos), ctl))) break;
           tc_fence_after();
           const uint32_t vb = sKV + s * C::kHalfBytes;
 #pragma unroll
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
         tc_commit(bar_pv_done);
         if (j + 2 < n_tiles) {
           // the next scores of this buffer overwrite P_j: once O += P V has read it
-          if (!(ok = mbar_wait(bar_pv_done, j & 1, ctl))) break;
+          if (!(ok = mbar_wait<kWaitParked>(bar_pv_done, j & 1, ctl))) break;
           tc_fence_after();
           ok = issue_qk(j + 2);
         }
@@ -235,8 +235,8 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
     if (j_pad >= 0) {
       const int pos = ld_v(j_pad);
       const bool ok = __all_sync(0xFFFFFFFFu, count_wait_sleep(pad_issued, 1u, ctl) &&
-                                                  mbar_wait(bar_kv_full(stage_of(pos)), phase_of(pos), ctl) &&
-                                                  mbar_wait(bar_kv_full(stage_of(pos + 1)), phase_of(pos + 1), ctl));
+                                                  mbar_wait<kWaitParked>(bar_kv_full(stage_of(pos)), phase_of(pos), ctl) &&
+                                                  mbar_wait<kWaitParked>(bar_kv_full(stage_of(pos + 1)), phase_of(pos + 1), ctl));
       if (ok) {  // both halves of V landed; their stages are refilled only after O += P V of them
         zero_padding_rows<128>(sKV + stage_of(pos) * C::kHalfBytes, kv_lim % kBlockN, lane, 32);
         zero_padding_rows<128>(sKV + stage_of(pos + 1) * C::kHalfBytes, kv_lim % kBlockN, lane, 32);
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
     float l = 0.0f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      ok = mbar_wait(bar_s_full(j & 1), bpar(j), ctl);
+      ok = mbar_wait<kWaitParked>(bar_s_full(j & 1), bpar(j), ctl);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
         break;
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
             // they are sequential, so the last one completing is enough.  The
             // parity wait is unambiguous: S_j exists, so the MMA thread has
             // seen tile j - 2's product complete, and tile j's waits for P_j.
-            ok = mbar_wait(bar_pv_done, (j - 1) & 1, ctl);
+            ok = mbar_wait<kWaitParked>(bar_pv_done, (j - 1) & 1, ctl);
             if (!__all_sync(0xFFFFFFFFu, ok)) {
               ok = false;
               break;
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
     }
     // ---- epilogue: O / l -> bf16, once every product has completed ---------
     if (ok && n_tiles > 0) {
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_drain, 0, ctl));
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait<kWaitParked>(bar_drain, 0, ctl));
       tc_fence_after();
     }
     if (ok) {
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
       }
       fence_proxy_async_smem();
       mbar_arrive(bar_o_staged);
-      if (t == 0 && mbar_wait(bar_o_staged, 0, ctl)) {
+      if (t == 0 && mbar_wait<kWaitParked>(bar_o_staged, 0, ctl)) {
         for (int c = 0; c < D / 64; ++c) tma_store_4d(&a.tm_o, sQ + c * C::kChunk, c * 64, h, q0, b);
         bulk_commit_group();
         bulk_wait_group_read0();  // the shared-memory source is read before the CTA retires

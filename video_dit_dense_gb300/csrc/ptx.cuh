@@ -80,16 +80,22 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
 }
 
 #ifndef H3ATTN_WAIT_MODE
-#define H3ATTN_WAIT_MODE 0  // 0: try_wait, 1: test_wait spin, 2: try_wait with a short suspend hint
+#define H3ATTN_WAIT_MODE 0  // default poll of mbar_wait (see kWaitPoll ...)
 #endif
+// How a barrier wait polls: kWaitPoll, try_wait (the thread may be suspended
+// for a system-dependent time); kWaitSpin, test_wait; kWaitShortHint,
+// try_wait with a 20 ns suspend hint; kWaitParked, try_wait with a 1 ms hint
+// (the thread sleeps in the wait until the phase completes).  Measured per
+// kernel: the one-query-tile kernel runs fastest with kWaitPoll (parked:
+// -3 % on long sequences), the two-CTA and head-dim-256 kernels with
+// kWaitParked (+2-3 %).
+constexpr int kWaitPoll = 0, kWaitSpin = 1, kWaitShortHint = 2, kWaitParked = 3;
+template <int MODE = H3ATTN_WAIT_MODE>
 __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
-#if H3ATTN_WAIT_MODE == 1
-  return mbar_test_wait(bar, parity);
-#elif H3ATTN_WAIT_MODE == 2
-  return mbar_try_wait_hint(bar, parity, 20);
-#else
+  if constexpr (MODE == kWaitSpin) return mbar_test_wait(bar, parity);
+  if constexpr (MODE == kWaitShortHint) return mbar_try_wait_hint(bar, parity, 20);
+  if constexpr (MODE == kWaitParked) return mbar_try_wait_hint(bar, parity, 1000000);
   return mbar_try_wait(bar, parity);
-#endif
 }
 
 // Shared abort/timeout bookkeeping of one CTA.
@@ -100,12 +106,13 @@ struct WaitCtl {
   int timeout_code;               // value written to *status on timeout
 };
 
+template <int MODE = H3ATTN_WAIT_MODE>
 __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_poll(bar, parity)) return true;
+      if (mbar_poll<MODE>(bar, parity)) return true;
     if (*ctl.abort_flag) return false;
     if (globaltimer_ns() - t0 > ctl.limit_ns) {
       *ctl.abort_flag = 1u;
@@ -117,9 +124,10 @@ __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, co
 
 // Wait until the phase with parity `parity` of `bar` has completed.
 // Returns false if the CTA is aborting (this waiter or another timed out).
+template <int MODE = H3ATTN_WAIT_MODE>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
-  if (mbar_poll(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, ctl);
+  if (mbar_poll<MODE>(bar, parity)) return true;
+  return mbar_wait_slow<MODE>(bar, parity, ctl);
 }
 
 __device__ __forceinline__ void fence_barrier_init() {
