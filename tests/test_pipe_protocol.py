@@ -459,6 +459,163 @@ def test_two_tile_kernel_needs_the_wait_before_the_next_score_product():
     assert bad > 0
 
 
+def run_separate_p(n_tiles, nstage, seed, pad_tile=None, s_read_wait=True):
+    """One random interleaving of the two-CTA kernel's head-dim-64 form
+    (attn_fwd, one query tile, P in a tensor-memory buffer of its own): the
+    producer loads Q, then K_j, V_j into an nstage ring; the MMA thread issues
+    S = Q K_0^T, then per key tile j: S = Q K_{j+1}^T once K_{j+1} has landed
+    and the softmax has read S_j out (s_read), then O += P_j V_j once V_j has
+    landed and P_j is published.  The softmax per tile waits for S_j, may
+    rescale O (after the previous P V), arrives s_read, waits for the previous
+    P V before writing P_j over the P buffer, publishes it; the epilogue waits
+    for the last P V.  s_read_wait=False drops the MMA thread's s_read wait
+    (a planted mistake).  Returns the list of protocol violations."""
+    rng = random.Random(seed)
+    q_full = Bar()
+    kv_full = [Bar() for _ in range(nstage)]
+    kv_empty = [Bar() for _ in range(nstage)]
+    s_full, s_read, p_ready, pv_done, v_clean = Bar(), Bar(), Bar(), Bar(), Bar()
+    st = {"Q": False, "stage": [None] * nstage, "S": None, "P": None, "O": 0, "pad_issued": False,
+          "zeroed": None}
+    queue, copies, errors = [], [], []
+
+    def producer():
+        copies.append(("Q", None))
+        for ld in range(2 * n_tiles):
+            sidx, ph = ld % nstage, (ld // nstage) & 1
+            yield lambda sidx=sidx, ph=ph: kv_empty[sidx].ok(ph ^ 1)
+            what = ("K" if ld % 2 == 0 else "V", ld // 2)
+            copies.append((sidx, what))
+            if what == ("V", pad_tile):
+                st["pad_issued"] = True
+
+    def pad_warp():
+        ld = 2 * pad_tile + 1
+        sidx, ph = ld % nstage, (ld // nstage) & 1
+        yield lambda: st["pad_issued"]
+        yield lambda: kv_full[sidx].ok(ph)
+        if st["stage"][sidx] != ("V", pad_tile):
+            errors.append(f"padding warp zeroes stage {sidx} holding {st['stage'][sidx]}")
+        st["zeroed"] = pad_tile
+        v_clean.arrive()
+
+    def mma():
+        yield lambda: q_full.ok(0)
+
+        def qk(j):
+            sk, phk = (2 * j) % nstage, ((2 * j) // nstage) & 1
+            yield lambda: kv_full[sk].ok(phk)
+            if j > 0 and s_read_wait:
+                yield lambda: s_read.ok((j - 1) & 1)
+            queue.extend([("qk", j, sk), ("commit", s_full), ("commit", kv_empty[sk])])
+
+        if n_tiles:
+            yield from qk(0)
+        for j in range(n_tiles):
+            if j + 1 < n_tiles:
+                yield from qk(j + 1)
+            sv, phv = (2 * j + 1) % nstage, ((2 * j + 1) // nstage) & 1
+            yield lambda: kv_full[sv].ok(phv)
+            if j == pad_tile:
+                yield lambda: v_clean.ok(0)
+            yield lambda: p_ready.ok(j & 1)
+            queue.extend([("pv", j, sv), ("commit", pv_done), ("commit", kv_empty[sv])])
+
+    def softmax():
+        for j in range(n_tiles):
+            yield lambda: s_full.ok(j & 1)
+            if st["S"] != j:
+                errors.append(f"softmax reads S holding {st['S']} for tile {j}")
+            if j > 0 and rng.random() < 0.5:   # the running max grew: rescale O
+                yield lambda: pv_done.ok((j - 1) & 1)
+                if st["O"] != j:
+                    errors.append(f"softmax rescales O holding {st['O']} tiles at tile {j}")
+            st["S"] = ("read", j)
+            s_read.arrive()
+            if j > 0:
+                yield lambda: pv_done.ok((j - 1) & 1)
+            if st["O"] != j:
+                errors.append(f"softmax writes P of tile {j} before O += P V of tile {j - 1} read the buffer")
+            st["P"] = j
+            p_ready.arrive()
+        if n_tiles:
+            yield lambda: pv_done.ok((n_tiles - 1) & 1)
+            if st["O"] != n_tiles:
+                errors.append(f"epilogue reads O holding {st['O']} of {n_tiles} tiles")
+
+    def execute():
+        op = take_tensor_op(queue, rng)
+        if op[0] == "commit":
+            op[1].arrive()
+            return
+        kind, j, sidx = op
+        if kind == "qk":
+            if not st["Q"]:
+                errors.append(f"S of tile {j} reads Q before it landed")
+            if st["stage"][sidx] != ("K", j):
+                errors.append(f"S of tile {j} reads stage {sidx} holding {st['stage'][sidx]}")
+            if isinstance(st["S"], int):
+                errors.append(f"S of tile {j} overwrites unread scores of tile {st['S']}")
+            st["S"] = j
+        else:
+            if st["stage"][sidx] != ("V", j):
+                errors.append(f"O += P V of tile {j} reads stage {sidx} holding {st['stage'][sidx]}")
+            if j == pad_tile and st["zeroed"] != j:
+                errors.append(f"O += P V of tile {j} reads V before its padding rows were zeroed")
+            if st["P"] != j or st["O"] != j:
+                errors.append(f"O += P V of tile {j} reads P {st['P']} onto O of {st['O']} tiles")
+            st["O"] = j + 1
+
+    roles = {"producer": producer(), "mma": mma(), "softmax": softmax()}
+    if pad_tile is not None:
+        roles["pad"] = pad_warp()
+    waits = {}
+    for name in list(roles):
+        try:
+            waits[name] = next(roles[name])
+        except StopIteration:
+            del roles[name]
+    while roles or queue or copies:
+        moves = [("role", r) for r in roles if waits[r]()]
+        if queue:
+            moves.append(("tensor", None))
+        moves += [("copy", i) for i in range(len(copies))]
+        if not moves:
+            return [f"deadlock: {sorted(roles)} waiting"]
+        kind, x = rng.choice(moves)
+        if kind == "role":
+            try:
+                waits[x] = roles[x].send(None)
+            except StopIteration:
+                del roles[x]
+        elif kind == "tensor":
+            execute()
+        else:
+            sidx, what = copies.pop(x)
+            if sidx == "Q":
+                st["Q"] = True
+                q_full.arrive()
+            else:
+                st["stage"][sidx] = what
+                kv_full[sidx].arrive()
+        if errors:
+            return errors
+    return errors
+
+
+@pytest.mark.parametrize("nstage", [3, 4, 6])
+def test_separate_p_protocol_is_clean(nstage):
+    for n in (1, 2, 3, 5, 16):
+        for trial in range(80):
+            pad = None if trial % 3 == 0 else trial % n
+            assert run_separate_p(n, nstage, trial, pad_tile=pad) == [], f"n {n}, pad {pad}, seed {trial}"
+
+
+def test_separate_p_needs_the_scores_read_wait():
+    bad = sum(bool(run_separate_p(8, 4, trial, s_read_wait=False)) for trial in range(300))
+    assert bad > 0
+
+
 def run_wide(n_tiles, nstage, seed, pad_tile=None, epilogue="drain"):
     """One random interleaving of the head-dim-256 kernel (attn_wide): score
     buffers S_0, S_1 (tile j in S_{j mod 2}, P_j written over it), O in two

@@ -62,7 +62,7 @@ struct Cfg {
   static constexpr int kChunkBytes = kBlockM * 128;       // 16 KiB: one swizzle column of a tile
   static constexpr int kSmemQ = NQ * kTileBytes;
   static constexpr int kSmemKV = NSTAGE * kTileBytes;
-  static constexpr int kNumBars = 1 + 2 * NSTAGE + 4 * NQ + 2;
+  static constexpr int kNumBars = 1 + 2 * NSTAGE + 4 * NQ + 3;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kSmemQ + kSmemKV + kNumBars * 8 + 16;
   // NQ softmax warpgroups + one control warpgroup (producer, MMA issuer, the warp that zeroes V
   // padding rows, one idle warp)
@@ -81,11 +81,17 @@ struct Cfg {
   // Only needed when the launch budget per thread is below what softmax wants.
   static constexpr bool kRebalance = kLaunchRegs < 200;
   static constexpr int kColO = NQ * 128;
+  // Head dim 64 with one query tile: P gets tensor-memory columns of its own
+  // after O (S 128 + O 64 + P 64 = the CTA's 256), so the next tile's scores
+  // may overwrite S as soon as the softmax has read it, instead of after the
+  // P V that reads P over S.
+  static constexpr bool kSepP = D == 64 && NQ == 1;
+  static constexpr int kColP = kColO + NQ * D;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kBlockN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
   // tensor memory per CTA: all of it, or an equal share (a power of two >= 32 columns)
   static constexpr uint32_t kTmemAlloc = CTAS == 1 ? kTmemCols : kTmemCols / CTAS;
-  static_assert(kColO + NQ * D <= static_cast<int>(kTmemAlloc), "tensor memory budget");
+  static_assert(kColO + NQ * D + (kSepP ? 64 : 0) <= static_cast<int>(kTmemAlloc), "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(CTAS * (kSmemBytes + 1024) <= 233472, "shared memory of CTAS resident CTAs");
 };
@@ -242,6 +248,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
   const uint32_t bar_v_clean = bars + 8u * (2 + 2 * NSTAGE + 3 * NQ);  // padding rows of V zeroed
   // o rows of query tile q staged for the TMA store (its 128 softmax threads)
   auto bar_o_staged = [&](int q) { return bars + 8u * (3 + 2 * NSTAGE + 3 * NQ + q); };
+  // separate-P form: the softmax has read the scores out of S (128 softmax threads)
+  const uint32_t bar_s_read = bars + 8u * (3 + 2 * NSTAGE + 4 * NQ);
   uint8_t* gmisc = gbase + C::kSmemQ + C::kSmemKV + C::kNumBars * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gmisc + 4);
@@ -286,6 +294,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
       mbar_init(bar_pv_done(q), 1);
       mbar_init(bar_o_staged(q), 128);
     }
+    mbar_init(bar_s_read, 128);
     mbar_init(bar_drain, 1);
     mbar_init(bar_v_clean, 1);
     *abort_flag = 0u;
@@ -357,6 +366,45 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
     if (lane == 0 && n_tiles > 0) {
       bool ok = mbar_wait<kWaitParked>(bar_q_full, 0, ctl);
       tc_fence_after();
+      if constexpr (C::kSepP) {
+        // S = Q K_0^T; then per key tile j: S = Q K_{j+1}^T once the softmax
+        // has read S_j out, and O += P_j V_j (A = P in its own columns).
+        // Ring positions: K_j at 2j, V_j at 2j + 1.
+        auto issue_qk = [&](int j) -> bool {
+          const int s = (2 * j) % NSTAGE;
+          if (!mbar_wait<kWaitParked>(bar_kv_full(s), ((2 * j) / NSTAGE) & 1, ctl)) return false;
+          if (j > 0 && !mbar_wait<kWaitParked>(bar_s_read, (j - 1) & 1, ctl)) return false;
+          tc_fence_after();
+          H3_TRACE(kEvMmaQK0, j);
+          const uint32_t kb = sKV + s * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+            mma_ss(tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), C::kIdescQK,
+                   kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar_s_full(0));
+          tc_commit(bar_kv_empty(s));
+          return true;
+        };
+        ok = ok && issue_qk(0);
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          if (j + 1 < n_tiles && !(ok = issue_qk(j + 1))) break;
+          const int s = (2 * j + 1) % NSTAGE;
+          if (!(ok = mbar_wait<kWaitParked>(bar_kv_full(s), ((2 * j + 1) / NSTAGE) & 1, ctl))) break;
+          if (j == j_pad && !(ok = mbar_wait<kWaitParked>(bar_v_clean, 0, ctl))) break;  // padding rows zeroed
+          if (!(ok = mbar_wait<kWaitParked>(bar_p_ready(0), j & 1, ctl))) break;
+          H3_TRACE(kEvMmaPV0, j);
+          tc_fence_after();
+          const uint32_t vb = sKV + s * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk)
+            mma_ts(tmem + C::kColO, tmem + C::kColP + kk * 8, sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024),
+                   C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar_pv_done(0));
+          tc_commit(bar_kv_empty(s));
+        }
+      } else {
       int it = 0;
       for (int j = 0; ok && j < n_tiles; ++j) {
         // S_q = Q_q K_j^T
@@ -411,6 +459,7 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
           if (!ok) break;
           tc_commit(bar_kv_empty(s));
         }
+      }
       }
       // Drain every MMA issued by this thread before tensor memory is freed.
       tc_commit(bar_drain);
@@ -490,8 +539,9 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
         m_ref = mt_s;
       }
       if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
-        // O_q += P V of the previous tile has completed before this tile's
-        // S_q was issued; the wait below returns at once and is kept as a guard.
+        // O_q holds every earlier product once O_q += P V of the previous
+        // tile has completed (P over S: before this tile's S_q was issued, so
+        // the wait returns at once; separate P: it may still be running).
         ok = mbar_wait<kWaitParked>(bar_pv_done(q), (j - 1) & 1, ctl);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
           ok = false;
@@ -525,8 +575,25 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
       }
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       if (t == 0) H3_TRACE(kEvSmExp0 + 4 * q, j);
-      tmem_st32(tS, p[0]);
-      tmem_st32(tS + 32, p[1]);
+      if constexpr (C::kSepP) {
+        // S is read out: the next tile's scores may overwrite it.  P's own
+        // buffer is free once O += P V of the previous tile has completed.
+        tc_fence_before();
+        mbar_arrive(bar_s_read);
+        if (j > 0) {
+          ok = mbar_wait<kWaitParked>(bar_pv_done(q), (j - 1) & 1, ctl);
+          if (!__all_sync(0xFFFFFFFFu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32(tmem + lane_off + C::kColP, p[0]);
+        tmem_st32(tmem + lane_off + C::kColP + 32, p[1]);
+      } else {
+        tmem_st32(tS, p[0]);
+        tmem_st32(tS + 32, p[1]);
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p_ready(q));
