@@ -91,7 +91,7 @@ struct Cfg {
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
   // tensor memory per CTA: all of it, or an equal share (a power of two >= 32 columns)
   static constexpr uint32_t kTmemAlloc = CTAS == 1 ? kTmemCols : kTmemCols / CTAS;
-  static_assert(kColO + NQ * D + (kSepP ? 64 : 0) <= static_cast<int>(kTmemAlloc), "tensor memory budget");
+  static_assert((kSepP ? kColP + 64 : kColO + NQ * D) <= static_cast<int>(kTmemAlloc), "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(CTAS * (kSmemBytes + 1024) <= 233472, "shared memory of CTAS resident CTAs");
 };
@@ -300,6 +300,22 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
     *abort_flag = 0u;
     *reinterpret_cast<volatile uint32_t*>(gmisc + 8) = 0u;  // pad_issued
     fence_barrier_init();
+    if (n_tiles > 0 && !a.debug_skip_producer) {
+      // Q and the first key tile's K and V (ring positions 0 and 1, first use
+      // of their stages) go out before the block-wide set-up completes
+      mbar_arrive_expect_tx(bar_q_full, C::kSmemQ);
+      for (int q = 0; q < NQ; ++q)
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sQ + q * C::kTileBytes + c * C::kChunkBytes, &a.tm_q, bar_q_full, c * 64, h,
+                      q0 + q * kBlockM, b);
+      for (int kind = 0; kind < 2; ++kind) {
+        mbar_arrive_expect_tx(bar_kv_full(kind), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sKV + kind * C::kTileBytes + c * C::kChunkBytes, kind == 0 ? &a.tm_k : &a.tm_v,
+                      bar_kv_full(kind), c * 64, kvh, 0, b);
+      }
+      if (j_pad == 0) st_release_cta(pad_issued, 1u);
+    }
     prefetch_tmap(&a.tm_q);
     prefetch_tmap(&a.tm_k);
     prefetch_tmap(&a.tm_v);
@@ -318,13 +334,8 @@ __global__ void __launch_bounds__(Cfg<D, NQ, NSTAGE, CTAS>::kThreads, CTAS)
    if (warp == C::kProducerWarp) {
     // ======================= TMA producer ==================================
     if (lane == 0 && n_tiles > 0 && !a.debug_skip_producer) {
-      mbar_arrive_expect_tx(bar_q_full, C::kSmemQ);
-      for (int q = 0; q < NQ; ++q)
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(sQ + q * C::kTileBytes + c * C::kChunkBytes, &a.tm_q, bar_q_full, c * 64, h,
-                      q0 + q * kBlockM, b);
-      int it = 0;
-      for (int j = 0; j < n_tiles; ++j) {
+      int it = 2;  // Q, K_0 and V_0 went out during the set-up
+      for (int j = 1; j < n_tiles; ++j) {
         bool ok = true;
         for (int kind = 0; kind < 2; ++kind, ++it) {
           const int s = it % NSTAGE;
