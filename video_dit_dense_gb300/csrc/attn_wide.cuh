@@ -130,8 +130,18 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
     *abort_flag = 0u;
     *reinterpret_cast<volatile uint32_t*>(gmisc + 8) = 0u;  // pad_issued
     fence_barrier_init();
-    prefetch_tmap(&a.tm_q);
-    prefetch_tmap(&a.tm_k);
+    if (n_tiles > 0 && !a.debug_skip_producer) {
+      // Q and the halves of K_0, K_1 (ring positions 0 .. 2 n_lead - 1, first
+      // use of their stages) go out before the block-wide set-up completes
+      mbar_arrive_expect_tx(bar_q_full, C::kQBytes);
+      for (int c = 0; c < D / 64; ++c) tma_load_4d(sQ + c * C::kChunk, &a.tm_q, bar_q_full, c * 64, h, q0, b);
+      for (int p = 0; p < 2 * n_lead; ++p) {
+        mbar_arrive_expect_tx(bar_kv_full(p), C::kHalfBytes);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sKV + p * C::kHalfBytes + c * C::kChunk, &a.tm_k, bar_kv_full(p), (2 * (p & 1) + c) * 64, kvh,
+                      tile_of(p >> 1) * kBlockN, b);
+      }
+    }
     prefetch_tmap(&a.tm_v);
   }
   if (warp == C::kMmaWarp) {
@@ -146,9 +156,7 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
   if (warp == C::kProducerWarp) {
     // ======================= TMA producer ==================================
     if (lane == 0 && n_tiles > 0 && !a.debug_skip_producer) {
-      mbar_arrive_expect_tx(bar_q_full, C::kQBytes);
-      for (int c = 0; c < D / 64; ++c) tma_load_4d(sQ + c * C::kChunk, &a.tm_q, bar_q_full, c * 64, h, q0, b);
-      int pos = 0;
+      int pos = 2 * n_lead;  // Q, K_0 and K_1 went out during the set-up
       bool ok = true;
       auto load = [&](int kind, int j) {  // both halves of K_j (kind 0) or V_j (kind 1)
         for (int half = 0; ok && half < 2; ++half) {
@@ -163,7 +171,6 @@ __global__ void __launch_bounds__(256, 1) attn_wide_kernel(const __grid_constant
         }
         if (ok && kind == 1 && j == j_pad) st_release_cta(pad_issued, 1u);
       };
-      for (int j = 0; ok && j < n_lead; ++j) load(0, j);
       for (int j = 0; ok && j < n_tiles; ++j) {
         load(1, j);
         if (ok && j + 2 < n_tiles) load(0, j + 2);
