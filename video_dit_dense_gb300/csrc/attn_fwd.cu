@@ -766,15 +766,16 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   //      keys on, and the chunked window;
   //   4  the two-tile kernel's code with one query tile per CTA, a short ring
   //      and two CTAs per SM (one CTA's prologue and epilogue overlap the
-  //      other's products): head_dim 128 below 1024 keys, head_dim 64;
+  //      other's products; at head_dim 64 P has tensor-memory columns of its
+  //      own): head_dim 128 below 1024 keys, head_dim 64;
   //   5  head_dim 256: one query tile per CTA with double-buffered scores
   //      (P over its score buffer, Q and half-tiles of K/V in shared memory);
   //   2  two query tiles per CTA sharing each K/V tile (head_dim 256: one
   //      tile with a single score buffer), only on request;
   //   3  the persistent kernel (one CTA per SM over all units), on request;
   //   6  head_dim 128: one CTA per SM chaining its work units (a unit's Q
-  //      load, scores and softmax overlap the previous unit's last products
-  //      and epilogue), on request.
+  //      hand-off and epilogue run on warps of their own beside the next
+  //      unit's tiles), on request.
   // a.kernel: 0 = by shape, else the kernel above (head dims it lacks fall
   // back to the shape rule's next choice).
   if (a.split_pieces > 0) {  // planned by plan_split: the one-query-tile kernel
