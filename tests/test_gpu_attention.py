@@ -283,3 +283,39 @@ def test_full_length_bit_mask_equals_structured_mask(h3):
     check_close(got.reshape(-1, wl.D)[ids], ref, "padded_gqa as bits")
     diff = (o_bits.float() - o_struct.float()).abs().max().item()
     assert diff <= 2e-2, f"bit-mask run differs from the structured run by {diff:.3e}"
+
+
+# The epilogues write o as whole 128-row tiles with TMA stores (rows past Sq
+# fall outside the tensor map and are dropped); the split tail's combine and
+# the zero rows of empty units write rows directly.  o here is a window into
+# a larger buffer whose bytes on both sides hold a sentinel: a write outside
+# o shows up there.
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,Sq,Sk,Hq,Hkv,D,split", [
+    (2, 300, 500, 3, 1, 128, False),   # ragged query tail, short keys (two CTAs per SM)
+    (1, 1100, 1100, 2, 2, 128, False),  # one query tile per CTA
+    (1, 1100, 1100, 2, 2, 128, True),   # ... with the split-key tail and its combine
+    (1, 77, 900, 2, 2, 64, False),
+    (2, 130, 260, 2, 1, 256, False),
+])
+def test_prefill_writes_nothing_outside_o(h3, kernel, B, Sq, Sk, Hq, Hkv, D, split):
+    import torch
+    q = gen.normal_bshd(B, Sq, Hq, D, 51, gen.STREAM_Q)
+    k = gen.normal_bshd(B, Sk, Hkv, D, 51, gen.STREAM_K)
+    v = gen.normal_bshd(B, Sk, Hkv, D, 51, gen.STREAM_V)
+    n, pad = B * Sq * Hq * D, 8192
+    sentinel = 0x7FA5  # a NaN pattern no kernel writes
+    buf = torch.full((pad + n + pad,), sentinel, dtype=torch.int16, device="cuda")
+    o = buf[pad:pad + n].view(torch.bfloat16).view(B, Sq, Hq, D)
+    ws = None
+    if split:
+        nbytes = h3.h3attn_prefill_workspace_size(B, Sq, Sk, Hq, Hkv, D)
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    h3.h3attn_prefill(to_dev(q), to_dev(k), to_dev(v), o, 1.0 / np.sqrt(D), workspace=ws)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    guard = torch.cat([buf[:pad], buf[pad + n:]])
+    assert bool((guard == sentinel).all()), "bytes outside o were written"
+    got = from_dev(o)
+    ref = oracle.attention_f64(q, k, v, 1.0 / np.sqrt(D))
+    check_close(got, ref, f"guarded o {B},{Sq},{Sk},{Hq},{Hkv},{D} split={split}")
