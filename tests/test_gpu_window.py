@@ -77,3 +77,27 @@ def test_window_packed_clip_sampled_rows(h3):
     ids = (rows[:, None] * wl.H + heads[None, :]).reshape(-1).astype(np.int64)
     ref = oracle.attention_window_f64(q, k, v, scale, *win, row_ids=ids)
     check_close(got.reshape(-1, wl.D)[ids], ref, "packed clip window, sampled rows")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,S,Hq,Hkv,D,win", [
+    (1, 700, 2, 2, 128, (16, 2, 5, 1)),
+    (2, 1000, 4, 2, 64, (50, 0, 3, 0)),
+])
+def test_window_writes_nothing_outside_o(h3, B, S, Hq, Hkv, D, win):
+    """o as a window into a larger buffer with sentinel bytes on both sides:
+    the epilogue's TMA stores of whole 128-row tiles stay inside o."""
+    import torch
+    q = gen.normal_bshd(B, S, Hq, D, 61, gen.STREAM_Q)
+    k = gen.normal_bshd(B, S, Hkv, D, 61, gen.STREAM_K)
+    v = gen.normal_bshd(B, S, Hkv, D, 61, gen.STREAM_V)
+    n, pad, sentinel = B * S * Hq * D, 8192, 0x7FA5
+    buf = torch.full((pad + n + pad,), sentinel, dtype=torch.int16, device="cuda")
+    o = buf[pad:pad + n].view(torch.bfloat16).view(B, S, Hq, D)
+    scale = 1.0 / np.sqrt(D)
+    h3.h3attn_prefill_window(to_dev(q), to_dev(k), to_dev(v), o, h3.Window(*win), scale)
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+    assert bool((torch.cat([buf[:pad], buf[pad + n:]]) == sentinel).all()), "bytes outside o were written"
+    ref = oracle.attention_window_f64(q, k, v, scale, *win)
+    check_close(from_dev(o), ref, f"guarded window o {B},{S},{Hq},{Hkv},{D},{win}")
