@@ -616,166 +616,6 @@ def test_separate_p_needs_the_scores_read_wait():
     assert bad > 0
 
 
-def run_split_scores(n_tiles, nstage, seed, pad_tile=None, wait_pv_before_second_half=True):
-    """One random interleaving of the two-CTA kernel's head-dim-128 form
-    (attn_fwd, one query tile, S of 128 columns with P over its second half):
-    the MMA thread computes each tile's scores as two 64-key halves, S_A =
-    Q K_j[0:64]^T into columns [0, 64) and S_B = Q K_j[64:128]^T into [64, 128).
-    Per key tile j: S_A of tile j + 1 once the softmax has read S_j out
-    (s_read); O += P_j V_j (P_j over S_B) once P_j is published; S_B of tile
-    j + 1 once that P V has completed, then s_full.  The softmax waits for
-    S_j, arrives s_read, may rescale O (after the previous P V), writes P_j
-    over S_B and publishes it.  wait_pv_before_second_half=False drops the
-    MMA thread's wait for the P V before S_B (a planted mistake).  Returns
-    the list of protocol violations."""
-    rng = random.Random(seed)
-    q_full = Bar()
-    kv_full = [Bar() for _ in range(nstage)]
-    kv_empty = [Bar() for _ in range(nstage)]
-    s_full, s_read, p_ready, pv_done, v_clean = Bar(), Bar(), Bar(), Bar(), Bar()
-    st = {"Q": False, "stage": [None] * nstage, "SA": None, "SB": None, "O": 0, "pad_issued": False,
-          "zeroed": None}
-    queue, copies, errors = [], [], []
-
-    def producer():
-        copies.append(("Q", None))
-        for ld in range(2 * n_tiles):
-            sidx, ph = ld % nstage, (ld // nstage) & 1
-            yield lambda sidx=sidx, ph=ph: kv_empty[sidx].ok(ph ^ 1)
-            what = ("K" if ld % 2 == 0 else "V", ld // 2)
-            copies.append((sidx, what))
-            if what == ("V", pad_tile):
-                st["pad_issued"] = True
-
-    def pad_warp():
-        ld = 2 * pad_tile + 1
-        sidx, ph = ld % nstage, (ld // nstage) & 1
-        yield lambda: st["pad_issued"]
-        yield lambda: kv_full[sidx].ok(ph)
-        if st["stage"][sidx] != ("V", pad_tile):
-            errors.append(f"padding warp zeroes stage {sidx} holding {st['stage'][sidx]}")
-        st["zeroed"] = pad_tile
-        v_clean.arrive()
-
-    def mma():
-        yield lambda: q_full.ok(0)
-        if not n_tiles:
-            return
-        sk, phk = 0, 0
-        yield lambda: kv_full[0].ok(0)
-        queue.extend([("qka", 0, 0), ("qkb", 0, 0), ("commit", s_full), ("commit", kv_empty[0])])
-        for j in range(n_tiles):
-            if j + 1 < n_tiles:
-                sk, phk = (2 * j + 2) % nstage, ((2 * j + 2) // nstage) & 1
-                yield lambda sk=sk, phk=phk: kv_full[sk].ok(phk)
-                yield lambda j=j: s_read.ok(j & 1)
-                queue.append(("qka", j + 1, sk))
-            sv, phv = (2 * j + 1) % nstage, ((2 * j + 1) // nstage) & 1
-            yield lambda sv=sv, phv=phv: kv_full[sv].ok(phv)
-            if j == pad_tile:
-                yield lambda: v_clean.ok(0)
-            yield lambda j=j: p_ready.ok(j & 1)
-            queue.extend([("pv", j, sv), ("commit", pv_done), ("commit", kv_empty[sv])])
-            if j + 1 < n_tiles:
-                if wait_pv_before_second_half:
-                    yield lambda j=j: pv_done.ok(j & 1)
-                queue.extend([("qkb", j + 1, sk), ("commit", s_full), ("commit", kv_empty[sk])])
-
-    def softmax():
-        for j in range(n_tiles):
-            yield lambda j=j: s_full.ok(j & 1)
-            if st["SA"] != j or st["SB"] != j:
-                errors.append(f"softmax reads S holding {st['SA']}, {st['SB']} for tile {j}")
-            st["SA"], st["SB"] = ("read", j), ("read", j)
-            s_read.arrive()
-            if j > 0 and rng.random() < 0.5:   # the running max grew: rescale O
-                yield lambda j=j: pv_done.ok((j - 1) & 1)
-                if st["O"] != j:
-                    errors.append(f"softmax rescales O holding {st['O']} tiles at tile {j}")
-            if st["SB"] != ("read", j):
-                errors.append(f"softmax writes P of tile {j} over S_B holding {st['SB']}")
-            st["SB"] = ("P", j)
-            p_ready.arrive()
-        if n_tiles:
-            yield lambda: pv_done.ok((n_tiles - 1) & 1)
-            if st["O"] != n_tiles:
-                errors.append(f"epilogue reads O holding {st['O']} of {n_tiles} tiles")
-
-    def execute():
-        op = take_tensor_op(queue, rng)
-        if op[0] == "commit":
-            op[1].arrive()
-            return
-        kind, j, sidx = op
-        if kind in ("qka", "qkb"):
-            half = "SA" if kind == "qka" else "SB"
-            if not st["Q"]:
-                errors.append(f"S of tile {j} reads Q before it landed")
-            if st["stage"][sidx] != ("K", j):
-                errors.append(f"S of tile {j} reads stage {sidx} holding {st['stage'][sidx]}")
-            cur = st[half]
-            if isinstance(cur, int) or (isinstance(cur, tuple) and cur[0] == "P" and st["O"] <= cur[1]):
-                errors.append(f"{half} of tile {j} overwrites {cur} before it was used")
-            st[half] = j
-        else:
-            if st["stage"][sidx] != ("V", j):
-                errors.append(f"O += P V of tile {j} reads stage {sidx} holding {st['stage'][sidx]}")
-            if j == pad_tile and st["zeroed"] != j:
-                errors.append(f"O += P V of tile {j} reads V before its padding rows were zeroed")
-            if st["SB"] != ("P", j) or st["O"] != j:
-                errors.append(f"O += P V of tile {j} reads S_B {st['SB']} onto O of {st['O']} tiles")
-            st["O"] = j + 1
-
-    roles = {"producer": producer(), "mma": mma(), "softmax": softmax()}
-    if pad_tile is not None:
-        roles["pad"] = pad_warp()
-    waits = {}
-    for name in list(roles):
-        try:
-            waits[name] = next(roles[name])
-        except StopIteration:
-            del roles[name]
-    while roles or queue or copies:
-        moves = [("role", r) for r in roles if waits[r]()]
-        if queue:
-            moves.append(("tensor", None))
-        moves += [("copy", i) for i in range(len(copies))]
-        if not moves:
-            return [f"deadlock: {sorted(roles)} waiting"]
-        kind, x = rng.choice(moves)
-        if kind == "role":
-            try:
-                waits[x] = roles[x].send(None)
-            except StopIteration:
-                del roles[x]
-        elif kind == "tensor":
-            execute()
-        else:
-            sidx, what = copies.pop(x)
-            if sidx == "Q":
-                st["Q"] = True
-                q_full.arrive()
-            else:
-                st["stage"][sidx] = what
-                kv_full[sidx].arrive()
-        if errors:
-            return errors
-    return errors
-
-
-@pytest.mark.parametrize("nstage", [2, 3, 4])
-def test_split_scores_protocol_is_clean(nstage):
-    for n in (1, 2, 3, 5, 16):
-        for trial in range(80):
-            pad = None if trial % 3 == 0 else trial % n
-            assert run_split_scores(n, nstage, trial, pad_tile=pad) == [], f"n {n}, pad {pad}, seed {trial}"
-
-
-def test_split_scores_needs_the_wait_before_the_second_half():
-    bad = sum(bool(run_split_scores(8, 2, trial, wait_pv_before_second_half=False)) for trial in range(300))
-    assert bad > 0
-
-
 def run_wide(n_tiles, nstage, seed, pad_tile=None, epilogue="drain"):
     """One random interleaving of the head-dim-256 kernel (attn_wide): score
     buffers S_0, S_1 (tile j in S_{j mod 2}, P_j written over it), O in two
