@@ -94,3 +94,35 @@ def test_index_outside_the_table_gives_zero_rows_and_an_error_status(h3):
     assert h3.h3attn_check_device_status() == 0  # the status word is cleared once read
     _assert_bits_equal(got, _expect(inp), "bad index rows")
     assert np.all(got[[2, 7]] == 0)
+
+
+# The kernel is launched as a programmatic dependent of the previous kernel
+# of the stream and reads or writes global memory only once that kernel has
+# completed.  Chained calls with no host synchronisation between them, each
+# reading what the one before wrote (out of place, in place, and after a
+# PyTorch kernel that rewrites the buffer), give the emulation applied in the
+# same order.
+@pytest.mark.gpu
+def test_back_to_back_calls_read_the_previous_output(h3):
+    import torch
+    inp = gen.make_modulate_inputs(20000, 3072, 4, seed=77)
+    w, idx = to_dev_f32(inp.w), to_dev_i32(inp.idx)
+    sc, sh = _dev2(inp.scale), _dev2(inp.shift)
+    x = _dev2(inp.x)
+    y = torch.full_like(x, float("nan"))
+    z = torch.full_like(x, float("nan"))
+    h3.h3attn_rmsnorm_modulate(x, y, w, sc, sh, idx, 1e-6)  # y = f(x)
+    h3.h3attn_rmsnorm_modulate(y, y, w, sc, sh, idx, 1e-6)  # y = f(f(x)), in place
+    y.neg_()                                                # a PyTorch kernel in between
+    h3.h3attn_rmsnorm_modulate(y, z, w, sc, sh, idx, 1e-6)  # z = f(-f(f(x)))
+    h3.h3attn_rmsnorm_modulate(z, x, w, sc, sh, idx, 1e-6)  # x = f(z), over the first input
+    torch.cuda.synchronize()
+    assert h3.h3attn_check_device_status() == 0
+
+    def f(bits):
+        return oracle.rmsnorm_modulate_emulate(bits, inp.w, inp.scale, inp.shift, inp.idx, 1e-6)
+    ref_y = f(f(inp.x)) ^ np.uint16(0x8000)
+    ref_z = f(ref_y)
+    _assert_bits_equal(from_dev(y), ref_y, "in place, then negated")
+    _assert_bits_equal(from_dev(z), ref_z, "after a PyTorch kernel")
+    _assert_bits_equal(from_dev(x), f(ref_z), "over the first call's input")

@@ -106,6 +106,12 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
   // staged norm weight: after the barriers and the abort word (16-byte aligned: row_bytes and 16 NS are)
   float* wsm = reinterpret_cast<float*>(smem + NS * row_bytes + 16 * NS + 16);
   WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns, static_cast<int>(H3ATTN_ERR_TIMEOUT)};
+  // Launched with programmatic stream serialization: the next kernel of the
+  // stream may be scheduled as soon as every CTA of this grid has started
+  // (its CTAs take an SM once one of these exits), and this grid touches
+  // global memory only after the previous kernel of the stream has completed
+  // (griddepcontrol.wait below; a no-op without the dependency).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int st = 0; st < NS; ++st) {
       mbar_init(bar_full(st), 1);
@@ -115,6 +121,7 @@ __global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 4 : 2)
     *reinterpret_cast<volatile uint32_t*>(smem + NS * row_bytes + 16 * NS + 4) = 0u;
     fence_barrier_init();
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (stage_w) {
     for (int i = threadIdx.x; i < (C >> 2); i += blockDim.x)
       reinterpret_cast<float4*>(wsm)[i] = __ldg(reinterpret_cast<const float4*>(a.w) + i);
@@ -235,8 +242,19 @@ cudaError_t launch_with(const ModArgs& a, int ctas_per_sm, int NS, int stage_w, 
   if (e != cudaSuccess) return e;
   int64_t blocks = static_cast<int64_t>(sms) * ctas_per_sm;
   if (blocks > a.T) blocks = a.T;
-  rmsnorm_modulate_kernel<W><<<static_cast<unsigned>(blocks), (W + 1) * 32, smem, stream>>>(a, NS, stage_w);
-  return cudaGetLastError();
+  // A programmatic dependent launch: back to back, the next launch's CTAs are
+  // placed while this one's last rows drain (+3 % at T 32760 x C 3072).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3((W + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rmsnorm_modulate_kernel<W>, a, NS, stage_w);
 }
 
 }  // namespace
