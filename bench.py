@@ -297,6 +297,11 @@ def run_gpu(args):
     for i in range(max(2, args.warmup)):
         e2e_step(i)
     barrier()
+    # the clocks of this region on their own: the copies draw power too
+    clocks_e2e = ClockSampler(local)
+    clocks_e2e.start()
+    barrier()
+    wall_e2e = time.time()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -306,6 +311,8 @@ def run_gpu(args):
     stream.wait_stream(s_out)
     e1.record(stream)
     barrier()
+    clocks_e2e.window(wall_e2e, time.time())
+    clk_e2e = clocks_e2e.stop()
     e2e_ms = e0.elapsed_time(e1)
 
     mod = _time_rmsnorm_modulate(h3, gen, torch, stream, peaks) if args.modulate else None
@@ -367,6 +374,8 @@ def run_gpu(args):
             "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
             "d2h_bytes_per_step": int(ho.numel() * 2),
             "ms_per_step": round(e2e_ms / args.steps, 4),
+            "clocks": {key: clk_e2e.get(key) for key in ("sm_mhz", "power_w_median", "power_w_max", "reasons",
+                                                         "samples", "window")},
         },
         "gpu_launches": ((1 if wl.norm_rope else 0) + attn_launches) * args.steps,
         "roofline": {
