@@ -269,6 +269,11 @@ h3attn_status_t h3attn_prefill_noalloc(const void* q, const void* k, const void*
  * C a multiple of 8, 8 <= C <= 8192; N >= 1; eps >= 0 and finite; T == 0 is a
  * no-op.  x, y, scale, shift, w 16-byte aligned, idx 4-byte aligned; y must not
  * overlap scale, shift, w, idx or (unless equal) x.
+ * Stream order as for any kernel.  The kernel is launched as a programmatic
+ * dependent of the kernel before it in the stream: it reads and writes memory
+ * only after that kernel has completed, while its CTAs may be placed as that
+ * kernel's last CTAs finish; a later launch that is itself a programmatic
+ * dependent may likewise start its set-up before this kernel ends.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_DEVICE, LAUNCH.
  */
 h3attn_status_t h3attn_rmsnorm_modulate(const void* x, void* y, const float* w, const void* scale,
