@@ -275,13 +275,18 @@ def run_gpu(args):
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step(i):
+    def e2e_step(i, tev=None):
+        # tev: timing events around this step's H2D and D2H on their streams
         bq, bk, bv, bo = bufs[i % 2]
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(ev_done[i % 2])
+            if tev:
+                tev[0].record(s_in)
             bq.copy_(hq, non_blocking=True); bk.copy_(hk, non_blocking=True); bv.copy_(hv, non_blocking=True)
             ev_in[i % 2].record(s_in)
+            if tev:
+                tev[1].record(s_in)
         stream.wait_event(ev_in[i % 2])
         if i >= 2:
             stream.wait_event(ev_out[i % 2])
@@ -291,8 +296,12 @@ def run_gpu(args):
         ev_done[i % 2].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_done[i % 2])
+            if tev:
+                tev[2].record(s_out)
             ho.copy_(bo, non_blocking=True)
             ev_out[i % 2].record(s_out)
+            if tev:
+                tev[3].record(s_out)
 
     for i in range(max(2, args.warmup)):
         e2e_step(i)
@@ -304,16 +313,19 @@ def run_gpu(args):
     wall_e2e = time.time()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    tevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     e0.record(stream)
     s_in.wait_event(e0)
     for i in range(args.steps):
-        e2e_step(i)
+        e2e_step(i, tevs[i])
     stream.wait_stream(s_out)
     e1.record(stream)
     barrier()
     clocks_e2e.window(wall_e2e, time.time())
     clk_e2e = clocks_e2e.stop()
     e2e_ms = e0.elapsed_time(e1)
+    h2d_ms = sum(t[0].elapsed_time(t[1]) for t in tevs) / args.steps
+    d2h_ms = sum(t[2].elapsed_time(t[3]) for t in tevs) / args.steps
 
     mod = _time_rmsnorm_modulate(h3, gen, torch, stream, peaks) if args.modulate else None
     wnd = _time_window(h3, gen, torch, stream, peaks) if args.window else None
@@ -374,6 +386,9 @@ def run_gpu(args):
             "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
             "d2h_bytes_per_step": int(ho.numel() * 2),
             "ms_per_step": round(e2e_ms / args.steps, 4),
+            # each step's copies on their own streams (they overlap the kernels)
+            "h2d_ms_per_step": round(h2d_ms, 4),
+            "d2h_ms_per_step": round(d2h_ms, 4),
             "clocks": {key: clk_e2e.get(key) for key in ("sm_mhz", "power_w_median", "power_w_max", "reasons",
                                                          "samples", "window")},
         },
