@@ -37,6 +37,7 @@ V, poisoned masked keys) and the fp64-vs-emulation rounding bound.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import hashlib
 import os
@@ -62,44 +63,73 @@ def build(force: bool = False) -> str:
             if f.read().strip() == h:
                 return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    # -ffp-contract=off: no implicit fused multiply-adds (the emulation's
-    # rounding order is part of its contract); no fast-math of any kind.
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-           "-fno-fast-math", "-pthread", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    _compile(_SRC, tmp)
     os.replace(tmp, _LIB)
     with open(stamp, "w") as f:
         f.write(h)
     return _LIB
 
 
+def _compile(src: str, out: str) -> None:
+    # -ffp-contract=off: no implicit fused multiply-adds (the emulation's
+    # rounding order is part of its contract); no fast-math of any kind.
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-pthread", src, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
+
+
+@contextlib.contextmanager
+def built_from(source: str, workdir: str):
+    """For the tests that plant a mistake in a copy of oracle.c: compile the
+    given C source with the flags of build() and route every call of this
+    module through that build inside the with-block."""
+    global _lib
+    src = os.path.join(workdir, "oracle_variant.c")
+    out = os.path.join(workdir, "liboracle_variant.so")
+    with open(src, "w") as f:
+        f.write(source)
+    _compile(src, out)
+    variant = _bind(ctypes.CDLL(out))
+    with _lock:
+        saved, _lib = _lib, variant
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = saved
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P, I64, I, D, F = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double,
-                               ctypes.c_float)
-            lib.oracle_qk_norm_rope_f64.argtypes = [P, P, I64, I, I, I, P, P, P, I, D, I, I]
-            lib.oracle_qk_norm_rope_emulate_bf16.argtypes = [P, P, I64, I, I, I, P, P, P, I, F, I]
-            lib.oracle_attention_f64.argtypes = [P, P, P, I, I, I, I, I, I, D, I, P, P, P, P, P,
-                                                 I64, P, I]
-            lib.oracle_round_f64_to_bf16.argtypes = [P, P, I64]
-            lib.oracle_rmsnorm_modulate_f64.argtypes = [P, P, I64, I, P, P, P, P, I, D, I]
-            lib.oracle_rmsnorm_modulate_emulate_bf16.argtypes = [P, P, I64, I, P, P, P, P, I, F, I]
-            lib.oracle_rmsnorm_modulate_f64.restype = None
-            lib.oracle_rmsnorm_modulate_emulate_bf16.restype = None
-            lib.oracle_allowed_pairs.argtypes = [I, I, I, I, P, P, P]
-            lib.oracle_allowed_pairs.restype = ctypes.c_int64
-            lib.oracle_attention_window_f64.argtypes = [P, P, P, I, I, I, I, I, D, I, I, I, I, P, P, P, I64, P, I]
-            lib.oracle_attention_window_f64.restype = None
-            lib.oracle_window_allowed_pairs.argtypes = [I, I, I, I, I, I]
-            lib.oracle_window_allowed_pairs.restype = ctypes.c_int64
-            for fn in ("oracle_qk_norm_rope_f64", "oracle_qk_norm_rope_emulate_bf16",
-                       "oracle_attention_f64", "oracle_round_f64_to_bf16"):
-                getattr(lib, fn).restype = None
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def _bind(lib):
+    """Declare the argument and result types of the oracle's C entry points."""
+    P, I64, I, D, F = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double,
+                       ctypes.c_float)
+    lib.oracle_qk_norm_rope_f64.argtypes = [P, P, I64, I, I, I, P, P, P, I, D, I, I]
+    lib.oracle_qk_norm_rope_emulate_bf16.argtypes = [P, P, I64, I, I, I, P, P, P, I, F, I]
+    lib.oracle_attention_f64.argtypes = [P, P, P, I, I, I, I, I, I, D, I, P, P, P, P, P,
+                                         I64, P, I]
+    lib.oracle_round_f64_to_bf16.argtypes = [P, P, I64]
+    lib.oracle_rmsnorm_modulate_f64.argtypes = [P, P, I64, I, P, P, P, P, I, D, I]
+    lib.oracle_rmsnorm_modulate_emulate_bf16.argtypes = [P, P, I64, I, P, P, P, P, I, F, I]
+    lib.oracle_rmsnorm_modulate_f64.restype = None
+    lib.oracle_rmsnorm_modulate_emulate_bf16.restype = None
+    lib.oracle_allowed_pairs.argtypes = [I, I, I, I, P, P, P]
+    lib.oracle_allowed_pairs.restype = ctypes.c_int64
+    lib.oracle_attention_window_f64.argtypes = [P, P, P, I, I, I, I, I, D, I, I, I, I, P, P, P, I64, P, I]
+    lib.oracle_attention_window_f64.restype = None
+    lib.oracle_window_allowed_pairs.argtypes = [I, I, I, I, I, I]
+    lib.oracle_window_allowed_pairs.restype = ctypes.c_int64
+    for fn in ("oracle_qk_norm_rope_f64", "oracle_qk_norm_rope_emulate_bf16",
+               "oracle_attention_f64", "oracle_round_f64_to_bf16"):
+        getattr(lib, fn).restype = None
+    return lib
 
 
 def _p(a):
